@@ -1,0 +1,88 @@
+"""The seeded input recipe (CPU only): the generator's quantiser against the
+oracle's independently written E4M3 encoder and ceil_to_ue8m0, and the group
+size draws of the five workloads."""
+import numpy as np
+import torch
+
+import oracle
+import synth
+from synth.inputs import CONFIGS, SA_KM, SA_MK, draw_group_sizes
+
+
+def test_quantiser_matches_oracle_encoding(oracle_mod):
+    gen = torch.Generator().manual_seed(123)
+    x = torch.randn(6, 384, generator=gen) * torch.tensor([1e-3, 1.0, 30.0]).repeat_interleave(128)
+    x[0, :128] = 0.0  # an all-zero block takes the amax floor
+    q, s = synth.quantize_a_blocks(x)
+    xs = x.double().numpy()
+    amax = np.maximum(np.abs(x.numpy()).reshape(6, 3, 128).max(axis=2), np.float32(1e-4))
+    t = (amax.astype(np.float32) / np.float32(448.0)).astype(np.float64)  # fp32 division
+    s_or = oracle.ceil_to_ue8m0(t)
+    assert np.array_equal(s.double().numpy(), s_or)
+    scaled = xs.reshape(6, 3, 128) / s_or[:, :, None]
+    assert np.all(np.abs(scaled) <= 448.0)
+    codes = oracle.e4m3_encode(scaled).reshape(6, 384)
+    same = (codes == q.numpy()) | (((codes & 0x7F) == 0) & ((q.numpy() & 0x7F) == 0))
+    assert same.all()
+
+
+def test_b_quantiser_blocks_are_128_by_128(oracle_mod):
+    gen = torch.Generator().manual_seed(5)
+    x = torch.randn(256, 256, generator=gen)
+    x[128:, 128:] *= 64.0  # one block much larger
+    q, s = synth.quantize_b_blocks(x)
+    assert s.shape == (2, 2)
+    assert s[1, 1] / s[0, 0] >= 32
+    deq = oracle.e4m3_decode(q.numpy()) * np.kron(s.double().numpy(), np.ones((128, 128)))
+    # e4m3 keeps 3 mantissa bits: relative error <= 2^-4 on normals
+    big = np.abs(x.numpy()) > 0.05 * np.abs(x.numpy()).max()
+    rel = np.abs(deq - x.double().numpy())[big] / np.abs(x.double().numpy())[big]
+    assert rel.max() <= 2.0 ** -4 + 1e-12
+
+
+def test_group_size_draws():
+    c3 = draw_group_sizes(CONFIGS["c3_contig_g8_mrand_n7168_k2304"]["sizes"], 8, 3)
+    assert len(c3) == 8 and all(100 <= m <= 1024 for m in c3)
+    c4 = draw_group_sizes(CONFIGS["c4_masked_g16_mmax1024_n2048_k7168"]["sizes"], 16, 4)
+    assert len(c4) == 16 and all(1 <= m <= 512 for m in c4)
+    c5 = draw_group_sizes(CONFIGS["c5_contig_g32_dirichlet_n4096_k7168"]["sizes"], 32, 5)
+    assert len(c5) == 32 and sum(c5) == 65536
+    assert draw_group_sizes(("fixed", 100), 2, 1) == [100, 100]
+    # deterministic
+    assert c5 == draw_group_sizes(CONFIGS["c5_contig_g32_dirichlet_n4096_k7168"]["sizes"], 32, 5)
+
+
+def test_contiguous_layout_and_scale_layouts():
+    p = synth.make_problem("contiguous", 3, 128, 256, [100, 0, 130], sa_layout=SA_KM, seed=7,
+                           tail_rows=5)
+    lay = p.grouped_layout.numpy()
+    assert p.row_offsets == [0, 128, 128, 384]
+    assert lay.size == 389
+    assert (lay[:100] == 0).all() and (lay[100:128] == -1).all()
+    assert (lay[128:258] == 2).all() and (lay[258:] == -1).all()
+    assert p.ld_sa % 4 == 0 and p.sa.shape == (2, p.ld_sa)
+    assert torch.equal(p.sa_mk(), p.sa[:, :389].t())
+    q = synth.make_problem("contiguous", 3, 128, 256, [100, 0, 130], sa_layout=SA_MK, seed=7,
+                           tail_rows=5)
+    assert torch.equal(q.a, p.a) and torch.equal(q.sa, p.sa_mk())
+
+
+def test_masked_problem_shapes():
+    p = synth.make_problem("masked", 2, 128, 128, [3, 0], M_max=5, sa_layout=SA_KM, seed=9)
+    assert p.a.shape == (2, 5, 128) and p.sa.shape == (2, 1, 8)
+    assert p.masked_m.tolist() == [3, 0]
+    assert p.group_of_row(2) == (0, 2) and p.group_of_row(3)[0] == -1
+    assert p.group_of_row(5)[0] == -1
+    v, u = synth.sample_rows(p, per_group=4)
+    assert set(v.tolist()) <= {0, 1, 2} and 3 in u.tolist()
+
+
+def test_sample_rows_cover_group_edges():
+    p = synth.make_problem("contiguous", 2, 128, 128, [100, 40], seed=3)
+    v, u = synth.sample_rows(p, per_group=8)
+    assert {0, 99, 128, 167}.issubset(set(v.tolist()))
+    assert {100, 127, 168, 255}.issubset(set(u.tolist()))
+    for r in v:
+        assert p.group_of_row(int(r))[0] >= 0
+    for r in u:
+        assert p.group_of_row(int(r))[0] == -1

@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Benchmark of the grouped FP8 block-scaled GEMM on GB300.
+
+One step = one call of the grouped GEMM over one batch of synthetic input
+(the whole path: scale staging, tile scheduling, TMA operand loads,
+block-scaled tcgen05 MMAs and the epilogue all run inside the one kernel the
+call launches).  The default workload is the contiguous G=8 x 1024-row,
+N=2048, K=7168 expert projection with transposed activation scales and bf16
+output.  Metric: TFLOP/s = 2 * sum(valid rows) * N * K / time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Under torchrun (N > 1) every rank runs an independent replica (the path has
+no exchange step), the timing is the max over ranks and `value` counts the
+work of all ranks.  Only rank 0 prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+DEFAULT_WORKLOAD = "c2_contig_g8_m1024_n2048_k7168"
+METRIC = "grouped FP8 GEMM TFLOP/s (2*sum(m)*N*K/t)"
+FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense tensor-core ratio of GB300
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "fp8_block_scaled_gb300", "csrc", f)
+                  for f in ("grouped_gemm.cuh", "ptx.cuh", "fp8bs_api.cu")]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ----------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms while running."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        bus = None
+        try:
+            props = torch.cuda.get_device_properties(self.device)
+            bus = getattr(props, "pci_bus_id", None)
+        except Exception:
+            pass
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        if rows and len({r[0] for r in rows}) > 1:
+            if bus is not None:
+                sel = [r for r in rows if r[1].lower().endswith(f"{int(bus):02x}:00.0")
+                       or f":{int(bus):02x}:" in r[1].lower()]
+                rows = sel or rows
+            idx = rows[0][0]
+            rows = [r for r in rows if r[0] == idx]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        smax = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- workloads
+def make_inputs(name: str, device):
+    import synth
+
+    return synth.make_config(name, device=device)
+
+
+def out_dtype_of(p):
+    return torch.bfloat16 if p.out_dtype == 0 else torch.float16
+
+
+def run_once(fb, p, a, sa, b, sb, rowinfo, d, stream=None):
+    if p.variant == "contiguous":
+        fb.gemm_grouped_contiguous(a, sa, b, sb, d, rowinfo, stream=stream)
+    else:
+        fb.gemm_grouped_masked(a, sa, b, sb, d, rowinfo, stream=stream)
+
+
+def describe(p, l2_note):
+    cfg = {"workload": p.name, "variant": p.variant, "G": p.G, "N": p.N, "K": p.K,
+           "valid_rows": p.valid_rows, "rows": p.rows,
+           "out": "bf16" if p.out_dtype == 0 else "f16",
+           "scale_a": "transposed [K/128, M]" if p.sa_layout == 1 else "[M, K/128]",
+           "scales": "UE8M0 (1,128) activation x (128,128) weight",
+           "parallelism": "replicas (no exchange step)", "l2": l2_note}
+    if p.variant == "masked":
+        cfg["M_max"] = p.M_max
+    return cfg
+
+
+def bench_ours(args):
+    import fp8_block_scaled_gb300 as fb
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    fb.load()
+    p = make_inputs(args.workload, dev)
+    sa_view = p.sa_mk_view()
+    rowinfo = p.grouped_layout if p.variant == "contiguous" else p.masked_m
+    in_bytes = sum(t.numel() * t.element_size() for t in (p.a, p.sa, p.b, p.sb, rowinfo))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sets = max(2, math.ceil(3 * l2 / in_bytes))
+    bufs = []
+    d_shape = (p.rows, p.N) if p.variant == "contiguous" else (p.G, p.M_max, p.N)
+    for i in range(sets):
+        if i == 0:
+            a, sa, b, sb, ri = p.a, sa_view, p.b, p.sb, rowinfo
+        else:
+            a, b, sb, ri = p.a.clone(), p.b.clone(), p.sb.clone(), rowinfo.clone()
+            sa_store = p.sa.clone()
+            if p.sa_layout == 1:
+                sa = (sa_store[:, : p.rows].t() if p.variant == "contiguous"
+                      else sa_store[:, :, : p.M_max].transpose(1, 2))
+            else:
+                sa = sa_store
+        d = torch.empty(d_shape, dtype=out_dtype_of(p), device=dev)
+        bufs.append((a, sa, b, sb, ri, d))
+    l2_note = (f"rotating {sets} input sets of {in_bytes / 1e6:.1f} MB "
+               f"({sets * in_bytes / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)")
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        run_once(fb, p, *bufs[i % sets])
+    torch.cuda.synchronize(dev)
+    if fb.device_error(local):
+        raise RuntimeError("device error word set during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        run_once(fb, p, *bufs[i % sets])
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if fb.device_error(local):
+        raise RuntimeError("device error word set during the timed region")
+    ms_per_step = max_over_ranks(elapsed_ms / args.steps, world, dev)
+    flops = p.flops()
+    total_flops = sum_over_ranks(flops, world, dev)
+    value = total_flops / (ms_per_step * 1e-3) / 1e12
+
+    # roofline of the one kernel on the path
+    peaks, peaks_kind = load_peaks()
+    mean_launch_ms = statistics.fmean(per_launch)
+    achieved = flops / (mean_launch_ms * 1e-3) / 1e12
+    peak_fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
+    alg_bytes = p.algorithmic_bytes(out_bytes=2)
+    hbm_time = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    tensor_time = flops / (peak_fp8 * 1e12)
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        ent = tr.get(p.name)
+        if ent and ent.get("kernel_hash") == kernel_hash():
+            traffic = ent["dram_bytes_per_launch"]
+    if tensor_time >= hbm_time:
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_fp8, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / peak_fp8, 4), "traffic": traffic,
+                "peak_source": f"{peaks_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
+                               f"{FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)",
+                "algorithmic": {"flops_per_launch": flops, "bytes_per_launch": alg_bytes},
+                "mean_launch_ms": round(mean_launch_ms, 5)}
+    else:
+        gbs = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": f"{peaks_kind} HBM copy",
+                "algorithmic": {"flops_per_launch": flops, "bytes_per_launch": alg_bytes},
+                "mean_launch_ms": round(mean_launch_ms, 5)}
+
+    # end to end through the public API with host buffers
+    e2e = bench_e2e(fb, p, dev, args.e2e_steps) if args.e2e_steps > 0 else None
+    if e2e is not None:
+        e2e_ms = max_over_ranks(e2e["ms_per_step"], world, dev)
+        e2e = {"value": round(total_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": e2e["h2d"],
+               "d2h_bytes_per_step": e2e["d2h"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        cpu = cpu_baseline(p, args.cpu_seconds)
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic (seeded N(0,1), UE8M0 ceil-quantised)",
+            "config": describe(p, l2_note), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clk,
+            "roofline_time_ms": {"tensor_at_peak": tensor_time * 1e3, "hbm_at_peak": hbm_time * 1e3}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_e2e(fb, p, dev, steps):
+    """Same metric through the public API, inputs in pinned host memory: each
+    step copies the inputs host->device, runs the GEMM and reads D back."""
+    rowinfo = p.grouped_layout if p.variant == "contiguous" else p.masked_m
+    host = [t.cpu().pin_memory() for t in (p.a, p.sa, p.b, p.sb, rowinfo)]
+    devb = [torch.empty_like(t, device=dev) for t in host]
+    d_shape = (p.rows, p.N) if p.variant == "contiguous" else (p.G, p.M_max, p.N)
+    d = torch.empty(d_shape, dtype=out_dtype_of(p), device=dev)
+    d_host = torch.empty(d_shape, dtype=out_dtype_of(p)).pin_memory()
+
+    def sa_view(sa):
+        if p.sa_layout == 0:
+            return sa
+        return sa[:, : p.rows].t() if p.variant == "contiguous" else sa[:, :, : p.M_max].transpose(1, 2)
+
+    def step():
+        for h, g in zip(host, devb):
+            g.copy_(h, non_blocking=True)
+        run_once(fb, p, devb[0], sa_view(devb[1]), devb[2], devb[3], devb[4], d)
+        d_host.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize(dev)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    return {"ms_per_step": t0.elapsed_time(t1) / steps, "h2d": h2d,
+            "d2h": d_host.numel() * d_host.element_size()}
+
+
+def _oracle_call(p, host, rows):
+    import oracle
+
+    a, sa, b, sb, ri = host
+    if p.variant == "contiguous":
+        return oracle.grouped_contiguous(a, sa, p.sa_layout, b, sb, ri, rows=rows, ld_sa=p.ld_sa)
+    return oracle.grouped_masked(a, sa, p.sa_layout, b, sb, ri, rows=rows, ld_sa=p.ld_sa)
+
+
+def _host_inputs(p):
+    rowinfo = p.grouped_layout if p.variant == "contiguous" else p.masked_m
+    return [t.cpu().numpy() for t in (p.a, p.sa, p.b, p.sb, rowinfo)]
+
+
+def _valid_row_list(p):
+    """Every valid (computed) row of the problem, as flattened row indices."""
+    rows = []
+    for g, m in enumerate(p.group_sizes):
+        base = p.row_offsets[g] if p.variant == "contiguous" else g * p.M_max
+        rows.extend(range(base, base + m))
+    return np.array(rows, dtype=np.int64)
+
+
+def cpu_baseline(p, seconds: float):
+    """The oracle as it stands, on the host cores, over a seeded row sample
+    sized to take about `seconds` of CPU time."""
+    import oracle
+
+    host = _host_inputs(p)
+    allrows = _valid_row_list(p)
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(allrows, size=min(len(allrows), 2 * oracle.max_threads()),
+                               replace=False))
+    t = time.perf_counter()
+    _oracle_call(p, host, probe)
+    per_row = (time.perf_counter() - t) / len(probe)
+    n = int(min(len(allrows), max(len(probe), seconds / max(per_row, 1e-9))))
+    rows = np.sort(rng.choice(allrows, size=n, replace=False))
+    t = time.perf_counter()
+    _oracle_call(p, host, rows)
+    dt = time.perf_counter() - t
+    flops = 2.0 * n * p.N * p.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{n} of {len(allrows)} valid rows (seeded), all N={p.N} columns, "
+                      f"{dt:.1f} s; fp64 C oracle, OpenMP over rows"}
+
+
+def bench_reference(args):
+    """Reference arm: the CPU oracle, timed as it stands, on the same workload
+    (each step a bounded seeded sample of its rows)."""
+    import oracle
+
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    p = make_inputs(args.workload, "cpu")
+    host = _host_inputs(p)
+    allrows = _valid_row_list(p)
+    rng = np.random.default_rng(1)
+    probe = np.sort(rng.choice(allrows, size=min(len(allrows), oracle.max_threads()), replace=False))
+    t = time.perf_counter()
+    _oracle_call(p, host, probe)
+    per_row = (time.perf_counter() - t) / len(probe)
+    budget = max(0.02, args.reference_seconds / max(1, args.steps + args.warmup))
+    rows_per_step = int(max(1, min(len(allrows), budget / max(per_row, 1e-9))))
+    samples = [np.sort(rng.choice(allrows, size=rows_per_step, replace=False))
+               for _ in range(min(8, args.steps + args.warmup))]
+    for i in range(args.warmup):
+        _oracle_call(p, host, samples[i % len(samples)])
+    t = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_call(p, host, samples[i % len(samples)])
+    dt = time.perf_counter() - t
+    flops = 2.0 * rows_per_step * p.N * p.K * args.steps
+    value = flops / dt / 1e12
+    ms = dt * 1e3 / args.steps
+    cpu = {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+           "kind": "oracle",
+           "sample": f"{rows_per_step} seeded valid rows x N={p.N} per step "
+                     f"(of {len(allrows)}); fp64 C oracle, OpenMP over rows"}
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), UE8M0)",
+            "config": describe(p, "n/a (CPU)"), "cpu_baseline": cpu,
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+"""ctypes binding of libfp8bs.so (argument marshalling only).
+
+Every tensor stays on the GPU; the library receives raw device pointers,
+sizes and the current CUDA stream.  There is no CPU fallback: if the library
+cannot be built or loaded, every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+
+SA_MK = 0
+SA_KM = 1
+OUT_BF16 = 0
+OUT_F16 = 1
+DEVERR_TIMEOUT = 0x1
+DEVERR_MASKED_M = 0x2
+DEVERR_MIXED_TILE = 0x4
+DEVERR_BAD_GROUP = 0x8
+
+# every symbol include/fp8bs.h declares
+EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "fp8bs_device_error",
+           "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class Fp8bsError(RuntimeError):
+    """A non-zero status from the C ABI."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(auto_build: bool = True) -> ctypes.CDLL:
+    """Load the CUDA library (building it in-tree with nvcc when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if auto_build and _build.is_stale():
+            _build.build()
+        if not os.path.exists(_build.LIB):
+            raise ImportError(f"fp8_block_scaled_gb300: CUDA library not built ({_build.LIB}); "
+                              "run fp8_block_scaled_gb300.build.build()")
+        lib = ctypes.CDLL(_build.LIB)
+        lib.gemm_grouped_contiguous.argtypes = [_P, _P, _I, _I64, _P, _P, _P, _P, _I,
+                                                _I64, _I64, _I64, _I64, _P]
+        lib.gemm_grouped_contiguous.restype = _I
+        lib.gemm_grouped_masked.argtypes = [_P, _P, _I, _I64, _P, _P, _P, _I64, _P, _I,
+                                            _I64, _I64, _I64, _I64, _P]
+        lib.gemm_grouped_masked.restype = _I
+        lib.fp8bs_device_error.argtypes = [_I, ctypes.POINTER(ctypes.c_uint32)]
+        lib.fp8bs_device_error.restype = _I
+        lib.fp8bs_status_string.argtypes = [_I]
+        lib.fp8bs_status_string.restype = ctypes.c_char_p
+        lib.fp8bs_clear_cache.argtypes = []
+        lib.fp8bs_clear_cache.restype = _I
+        lib.fp8bs_abi_version.argtypes = []
+        lib.fp8bs_abi_version.restype = _I
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    if _lib is None:
+        return "?"
+    return _lib.fp8bs_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise Fp8bsError(status, what)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _out_code(d: torch.Tensor) -> int:
+    if d.dtype == torch.bfloat16:
+        return OUT_BF16
+    if d.dtype == torch.float16:
+        return OUT_F16
+    raise TypeError("output must be bfloat16 or float16")
+
+
+def _fp8_ptr(t: torch.Tensor, name: str) -> int:
+    if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise TypeError(f"{name} must be float8_e4m3fn (or its uint8 codes)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _sa_layout_2d(sa: torch.Tensor, rows: int, kb: int):
+    """(layout, ld) of a logical [rows, K/128] scale tensor from its strides."""
+    if sa.dtype != torch.float32 or sa.shape != (rows, kb):
+        raise ValueError(f"scale_a must be fp32 [{rows}, {kb}], got {tuple(sa.shape)} {sa.dtype}")
+    s0, s1 = sa.stride()
+    if s1 == 1 and (s0 == kb or rows == 1):
+        return SA_MK, kb
+    if s0 == 1:
+        return SA_KM, s1
+    raise ValueError("scale_a must be row-major [M, K/128] or a transposed view of [K/128, ld]")
+
+
+def _sa_layout_3d(sa: torch.Tensor, G: int, m_max: int, kb: int):
+    if sa.dtype != torch.float32 or sa.shape != (G, m_max, kb):
+        raise ValueError(f"scale_a must be fp32 [{G}, {m_max}, {kb}], got {tuple(sa.shape)}")
+    s0, s1, s2 = sa.stride()
+    if s2 == 1 and s1 == kb and s0 == m_max * kb:
+        return SA_MK, kb
+    if s1 == 1 and s0 == kb * s2:
+        return SA_KM, s2
+    raise ValueError("scale_a must be [G, M_max, K/128] row-major or a transposed view of "
+                     "[G, K/128, ld]")
+
+
+def gemm_grouped_contiguous_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr, layout_ptr,
+                                d_ptr, out_dtype, m_sum, n, k, num_groups, stream=None) -> int:
+    """Direct C-ABI call with raw device pointers; returns the status code."""
+    lib = load()
+    return lib.gemm_grouped_contiguous(a_ptr, sa_ptr, int(sa_layout), int(ld_sa), b_ptr, sb_ptr,
+                                       layout_ptr, d_ptr, int(out_dtype), int(m_sum), int(n),
+                                       int(k), int(num_groups), ctypes.c_void_p(_stream_handle(stream)))
+
+
+def gemm_grouped_masked_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr, masked_m_ptr,
+                            expected_m, d_ptr, out_dtype, num_groups, m_max, n, k,
+                            stream=None) -> int:
+    lib = load()
+    return lib.gemm_grouped_masked(a_ptr, sa_ptr, int(sa_layout), int(ld_sa), b_ptr, sb_ptr,
+                                   masked_m_ptr, int(expected_m), d_ptr, int(out_dtype),
+                                   int(num_groups), int(m_max), int(n), int(k),
+                                   ctypes.c_void_p(_stream_handle(stream)))
+
+
+def gemm_grouped_contiguous(a, scale_a, b, scale_b, d, grouped_layout, *, stream=None):
+    """D = grouped FP8 block-scaled GEMM, contiguous variant (see include/fp8bs.h).
+
+    a [M_sum, K] e4m3; scale_a logical [M_sum, K/128] fp32 (row-major, or a
+    transposed view of a [K/128, ld] buffer); b [G, N, K] e4m3; scale_b
+    [G, N/128, K/128] fp32; d [M_sum, N] bf16/f16; grouped_layout [M_sum]
+    int32 with -1 for padding rows.  Rows marked -1 are not written.
+    """
+    m_sum, k = a.shape
+    G, n, kb_ = b.shape
+    if kb_ != k or d.shape != (m_sum, n) or grouped_layout.shape != (m_sum,):
+        raise ValueError("shape mismatch")
+    if scale_b.shape != (G, n // 128, k // 128) or scale_b.dtype != torch.float32:
+        raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
+    if grouped_layout.dtype != torch.int32 or not d.is_contiguous():
+        raise ValueError("grouped_layout must be int32, d contiguous")
+    for t in (a, scale_a, b, scale_b, d, grouped_layout):
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+    layout, ld = _sa_layout_2d(scale_a, m_sum, k // 128)
+    st = gemm_grouped_contiguous_raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld,
+                                     _fp8_ptr(b, "b"), scale_b.contiguous().data_ptr(),
+                                     grouped_layout.contiguous().data_ptr(), d.data_ptr(),
+                                     _out_code(d), m_sum, n, k, G, stream)
+    _check(st, "gemm_grouped_contiguous")
+    return d
+
+
+def gemm_grouped_masked(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0, *,
+                        stream=None):
+    """D = grouped FP8 block-scaled GEMM, masked variant (see include/fp8bs.h).
+
+    a [G, M_max, K] e4m3; scale_a logical [G, M_max, K/128] fp32 (row-major,
+    or a transposed view of a [G, K/128, ld] buffer); b [G, N, K]; scale_b
+    [G, N/128, K/128]; d [G, M_max, N]; masked_m [G] int32 on the device.
+    Rows m >= masked_m[g] are not written.
+    """
+    G, m_max, k = a.shape
+    Gb, n, kb_ = b.shape
+    if Gb != G or kb_ != k or d.shape != (G, m_max, n) or masked_m.shape != (G,):
+        raise ValueError("shape mismatch")
+    if scale_b.shape != (G, n // 128, k // 128) or scale_b.dtype != torch.float32:
+        raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
+    if masked_m.dtype != torch.int32 or not d.is_contiguous():
+        raise ValueError("masked_m must be int32, d contiguous")
+    for t in (a, scale_a, b, scale_b, d, masked_m):
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+    layout, ld = _sa_layout_3d(scale_a, G, m_max, k // 128)
+    st = gemm_grouped_masked_raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld,
+                                 _fp8_ptr(b, "b"), scale_b.contiguous().data_ptr(),
+                                 masked_m.contiguous().data_ptr(), expected_m, d.data_ptr(),
+                                 _out_code(d), G, m_max, n, k, stream)
+    _check(st, "gemm_grouped_masked")
+    return d
+
+
+def device_error(device: int = None) -> int:
+    """Synchronise the device and return (and clear) its FP8BS_DEVERR_* bits."""
+    lib = load()
+    if device is None:
+        device = torch.cuda.current_device()
+    flags = ctypes.c_uint32(0)
+    st = lib.fp8bs_device_error(int(device), ctypes.byref(flags))
+    if st not in (0, 4):
+        raise Fp8bsError(st, "fp8bs_device_error")
+    return int(flags.value)
+
+
+def clear_cache() -> None:
+    _check(load().fp8bs_clear_cache(), "fp8bs_clear_cache")
+
+
+def abi_version() -> int:
+    return int(load().fp8bs_abi_version())

@@ -1,0 +1,334 @@
+// C ABI of the grouped FP8 block-scaled GEMM (declared in include/fp8bs.h):
+// argument validation, the TMA tensor-map cache, per-device state and the
+// kernel launches.  The operation and its two variants are those of the page
+// "Adds Grouped and Batched GEMM kernels with blockscaling matching DeepGEMM
+// API" (FlyDSL PR #433), section Summary; the raw-pointer argument style
+// follows "flydsl mxfp4 a4w4 MoE: bring gemm1/gemm2 to parity with the HIP
+// backend" (aiter PR #3828), section Changes / ABI.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "fp8bs.h"
+#include "grouped_gemm.cuh"
+
+// Per-device error word written by the kernels (FP8BS_DEVERR_* bits).
+__device__ uint32_t g_fp8bs_error_word;
+
+namespace {
+
+using fp8bs::GemmParams;
+using fp8bs::SmemLayout;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int status = FP8BS_OK;      // FP8BS_ERR_UNSUPPORTED when the device is not sm_103
+    int sms = 0;
+    uint32_t* err = nullptr;    // device address of g_fp8bs_error_word
+    bool attr_set[16] = {};
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct MapKey {
+    int dev;
+    const void* ptr;
+    uint64_t inner, outer, box_outer;
+    bool operator<(const MapKey& o) const {
+        return std::tie(dev, ptr, inner, outer, box_outer) <
+               std::tie(o.dev, o.ptr, o.inner, o.outer, o.box_outer);
+    }
+};
+std::map<MapKey, CUtensorMap> g_maps;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Resolve the current device and its cached state (lock held by caller).
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        st.sms = sms;
+        st.status = (major == 10 && minor == 3) ? FP8BS_OK : FP8BS_ERR_UNSUPPORTED;
+        if (st.status == FP8BS_OK) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_fp8bs_error_word) != cudaSuccess) {
+                cudaGetLastError();
+                return FP8BS_ERR_CUDA;
+            }
+            st.err = static_cast<uint32_t*>(addr);
+        }
+        if (g_encode == nullptr) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr) {
+                cudaGetLastError();
+                return FP8BS_ERR_CUDA;
+            }
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        st.ready = true;
+    }
+    *out = &st;
+    return st.status;
+}
+
+// 2-D E4M3 tensor map: `outer` rows of `inner` bytes, box 128 bytes x box_outer
+// rows, 128-byte swizzle, out-of-range rows read as zero.
+int get_map(int dev, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer,
+            const CUtensorMap** out) {
+    MapKey key{dev, ptr, inner, outer, box_outer};
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+        *out = &it->second;
+        return FP8BS_OK;
+    }
+    CUtensorMap map;
+    std::memset(&map, 0, sizeof(map));
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner};  // bytes between rows
+    cuuint32_t box[2] = {128u, box_outer};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return FP8BS_ERR_CUDA;
+    if (g_maps.size() > 4096) g_maps.clear();
+    auto ins = g_maps.emplace(key, map);
+    *out = &ins.first->second;
+    return FP8BS_OK;
+}
+
+template <int BN, typename OutT, bool kMasked>
+int launch(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensorMap& tb,
+           const GemmParams& p, int64_t tiles_bound, cudaStream_t stream) {
+    using L = SmemLayout<BN>;
+    auto kern = fp8bs::grouped_gemm_kernel<BN, OutT, kMasked>;
+    const int smem = (kMasked ? L::kBytesMasked : L::kBytesContiguous) + L::kAlignSlack;
+    if (!st.attr_set[attr_slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        st.attr_set[attr_slot] = true;
+    }
+    const int grid = static_cast<int>(tiles_bound < st.sms ? tiles_bound : st.sms);
+    if (grid <= 0) return FP8BS_OK;
+    kern<<<grid, fp8bs::kThreads, smem, stream>>>(ta, tb, p);
+    return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+template <bool kMasked>
+int dispatch(DeviceState& st, int bn, int out_dtype, const CUtensorMap& ta, const CUtensorMap& tb,
+             const GemmParams& p, int64_t tiles_bound, cudaStream_t stream) {
+    const int slot = (kMasked ? 8 : 0) + (bn == 256 ? 4 : 0) + out_dtype;
+    if (bn == 256) {
+        return out_dtype == FP8BS_OUT_BF16
+                   ? launch<256, __nv_bfloat16, kMasked>(st, slot, ta, tb, p, tiles_bound, stream)
+                   : launch<256, __half, kMasked>(st, slot, ta, tb, p, tiles_bound, stream);
+    }
+    return out_dtype == FP8BS_OUT_BF16
+               ? launch<128, __nv_bfloat16, kMasked>(st, slot, ta, tb, p, tiles_bound, stream)
+               : launch<128, __half, kMasked>(st, slot, ta, tb, p, tiles_bound, stream);
+}
+
+// Checks shared by both variants; touches no CUDA state.
+int validate_common(const void* a, const float* sa, int sa_layout, int64_t ld_sa, const void* b,
+                    const float* sb, const void* d, int out_dtype, int64_t sa_rows, int64_t n,
+                    int64_t k, int64_t num_groups) {
+    if (n <= 0 || k <= 0 || n % 128 || k % 128) return FP8BS_ERR_INVALID_ARG;
+    if (num_groups < 1) return FP8BS_ERR_INVALID_ARG;
+    if (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16) return FP8BS_ERR_INVALID_ARG;
+    if (sa_layout != FP8BS_SA_MK && sa_layout != FP8BS_SA_KM) return FP8BS_ERR_INVALID_ARG;
+    if (!a || !sa || !b || !sb || !d) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(d, 16)) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned(sa, 4) || !aligned(sb, 4)) return FP8BS_ERR_INVALID_ARG;
+    if (sa_layout == FP8BS_SA_KM) {
+        if (ld_sa < sa_rows || ld_sa % 4 || !aligned(sa, 16)) return FP8BS_ERR_INVALID_ARG;
+    }
+    // TMA coordinates and tile indices are 32-bit
+    if (num_groups * n > INT32_MAX || k > INT32_MAX / 2) return FP8BS_ERR_INVALID_ARG;
+    return FP8BS_OK;
+}
+
+int pick_bn(int64_t n) { return n % 256 == 0 ? 256 : 128; }
+
+}  // namespace
+
+extern "C" {
+
+int fp8bs_abi_version(void) { return 1; }
+
+const char* fp8bs_status_string(int status) {
+    switch (status) {
+        case FP8BS_OK: return "ok";
+        case FP8BS_ERR_INVALID_ARG: return "invalid argument";
+        case FP8BS_ERR_UNSUPPORTED: return "unsupported device (needs compute capability 10.3)";
+        case FP8BS_ERR_CUDA: return "CUDA error";
+        case FP8BS_ERR_DEVICE: return "device error word set";
+        default: return "unknown status";
+    }
+}
+
+int fp8bs_clear_cache(void) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_maps.clear();
+    return FP8BS_OK;
+}
+
+int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, int64_t ld_sa,
+                            const void* b, const float* scale_b, const int32_t* grouped_layout,
+                            void* d, int out_dtype, int64_t m_sum, int64_t n, int64_t k,
+                            int64_t num_groups, void* stream) {
+    if (m_sum < 0 || m_sum > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (m_sum == 0) {
+        // nothing to compute; still reject malformed sizes and codes
+        if (n <= 0 || k <= 0 || n % 128 || k % 128 || num_groups < 1 ||
+            (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16) ||
+            (sa_layout != FP8BS_SA_MK && sa_layout != FP8BS_SA_KM))
+            return FP8BS_ERR_INVALID_ARG;
+        return FP8BS_OK;
+    }
+    int v = validate_common(a, scale_a, sa_layout, ld_sa, b, scale_b, d, out_dtype, m_sum, n, k,
+                            num_groups);
+    if (v != FP8BS_OK) return v;
+    if (!grouped_layout || !aligned(grouped_layout, 4)) return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int bn = pick_bn(n);
+    const CUtensorMap *ta = nullptr, *tb = nullptr;
+    if ((rc = get_map(dev, a, k, m_sum, 128, &ta)) != FP8BS_OK) return rc;
+    if ((rc = get_map(dev, b, k, num_groups * n, bn, &tb)) != FP8BS_OK) return rc;
+
+    GemmParams p{};
+    p.sa = scale_a;
+    p.sb = scale_b;
+    p.row_info = grouped_layout;
+    p.d = d;
+    p.err = st->err;
+    p.rows = m_sum;
+    p.sa_g_stride = 0;
+    p.sa_kb_stride = sa_layout == FP8BS_SA_KM ? ld_sa : 1;
+    p.sa_row_stride = sa_layout == FP8BS_SA_KM ? 1 : k / 128;
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(k / 128);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>((m_sum + 127) / 128);
+    p.num_n_tiles = static_cast<int>(n / bn);
+    p.raster_band = 8;
+    const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+    return dispatch<false>(*st, bn, out_dtype, *ta, *tb, p, tiles,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int64_t ld_sa,
+                        const void* b, const float* scale_b, const int32_t* masked_m,
+                        int64_t expected_m, void* d, int out_dtype, int64_t num_groups,
+                        int64_t m_max, int64_t n, int64_t k, void* stream) {
+    (void)expected_m;  // scheduling hint only; results never depend on it
+    if (m_max < 0 || num_groups < 1 || num_groups > fp8bs::kMaxMaskedGroups)
+        return FP8BS_ERR_INVALID_ARG;
+    if (m_max > 0 && num_groups * m_max > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (m_max == 0) {
+        if (n <= 0 || k <= 0 || n % 128 || k % 128 ||
+            (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16) ||
+            (sa_layout != FP8BS_SA_MK && sa_layout != FP8BS_SA_KM))
+            return FP8BS_ERR_INVALID_ARG;
+        return FP8BS_OK;
+    }
+    int v = validate_common(a, scale_a, sa_layout, ld_sa, b, scale_b, d, out_dtype, m_max, n, k,
+                            num_groups);
+    if (v != FP8BS_OK) return v;
+    if (!masked_m || !aligned(masked_m, 4)) return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int bn = pick_bn(n);
+    const CUtensorMap *ta = nullptr, *tb = nullptr;
+    if ((rc = get_map(dev, a, k, num_groups * m_max, 128, &ta)) != FP8BS_OK) return rc;
+    if ((rc = get_map(dev, b, k, num_groups * n, bn, &tb)) != FP8BS_OK) return rc;
+
+    const int64_t kb = k / 128;
+    GemmParams p{};
+    p.sa = scale_a;
+    p.sb = scale_b;
+    p.row_info = masked_m;
+    p.d = d;
+    p.err = st->err;
+    p.rows = m_max;
+    p.sa_g_stride = sa_layout == FP8BS_SA_KM ? kb * ld_sa : m_max * kb;
+    p.sa_kb_stride = sa_layout == FP8BS_SA_KM ? ld_sa : 1;
+    p.sa_row_stride = sa_layout == FP8BS_SA_KM ? 1 : kb;
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(kb);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>((m_max + 127) / 128);
+    p.num_n_tiles = static_cast<int>(n / bn);
+    p.raster_band = 1;
+    const int64_t tiles = num_groups * p.num_m_tiles * p.num_n_tiles;
+    return dispatch<true>(*st, bn, out_dtype, *ta, *tb, p, tiles,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int fp8bs_device_error(int device, uint32_t* flags) {
+    if (!flags || device < 0 || device >= kMaxDevices) return FP8BS_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int old = 0;
+    if (cudaGetDevice(&old) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    int rc = FP8BS_OK;
+    uint32_t value = 0;
+    const uint32_t zero = 0;
+    if (cudaSetDevice(device) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&value, g_fp8bs_error_word, sizeof(value)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_fp8bs_error_word, &zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        rc = FP8BS_ERR_CUDA;
+    }
+    cudaSetDevice(old);
+    *flags = value;
+    if (rc == FP8BS_OK && value != 0) rc = FP8BS_ERR_DEVICE;
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+/*
+ * fp8bs.h -- C ABI of the GB300 (sm_103a) grouped FP8 block-scaled GEMM.
+ *
+ * The operation ("Adds Grouped and Batched GEMM kernels with blockscaling
+ * matching DeepGEMM API", FlyDSL PR #433, section Summary):
+ *
+ *   D[r, n] = sum_kb  scale_a[r, kb] * scale_b[g, n/128, kb]
+ *                     * sum_{k = 128*kb}^{128*kb+127} A[r, k] * B[g, n, k]
+ *
+ * with A and B in FP8 E4M3 (OCP "FN" encoding), one activation scale per
+ * (1 row, 128 K) block and one weight scale per (128 N, 128 K) block, fp32
+ * accumulation and a bf16 or f16 output rounded to nearest even.  g is the
+ * group (MoE expert) of row r.  Both operands are K-major ("NT"): A row r is
+ * K contiguous bytes, B[g] row n is K contiguous bytes.
+ *
+ * Scales are fp32 values that must be powers of two in [2^-127, 2^127]
+ * (UE8M0: the page's section "DeepGEMM conformance details" rounds them with
+ * ceil_to_ue8m0 and has the matrix instruction apply them).  The kernels use
+ * the fp32 exponent field as the UE8M0 scale byte; a scale that is not a
+ * power of two is truncated to the power of two below it.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *    contiguous unless a leading dimension says otherwise.  The library keeps
+ *    none of them past the call except as a key of its tensor-map cache.
+ *  - A, B and D must be 16-byte aligned; scale tensors 4-byte aligned (16-byte
+ *    for the transposed activation-scale layout, whose ld_sa must be a
+ *    multiple of 4).  N and K must be positive multiples of 128.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous: they validate, enqueue one kernel and return.  Nothing is
+ *    allocated on the device.
+ *  - Rows that are not computed (grouped_layout == -1, or m >= masked_m[g])
+ *    are not written: D keeps its prior contents there.
+ *  - Return value: FP8BS_OK, or an error code; nothing is enqueued on error.
+ *    Device-side problems (masked_m out of range, a 128-row tile holding two
+ *    experts, a pipeline wait that exceeded its time limit) are recorded in a
+ *    per-device error word read by fp8bs_device_error().
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum fp8bs_status {
+    FP8BS_OK = 0,
+    FP8BS_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment, layout or dtype code */
+    FP8BS_ERR_UNSUPPORTED = 2, /* device is not compute capability 10.x / sm_103 family */
+    FP8BS_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+    FP8BS_ERR_DEVICE = 4       /* fp8bs_device_error(): the device error word was set */
+};
+
+enum fp8bs_out_dtype { FP8BS_OUT_BF16 = 0, FP8BS_OUT_F16 = 1 };
+
+/* Activation-scale layouts (page section Summary: "including the transposed
+ * [scale_k, M] activation-scale layout"). */
+enum fp8bs_sa_layout {
+    FP8BS_SA_MK = 0, /* [rows, K/128] row-major (per group [M_max, K/128] when masked) */
+    FP8BS_SA_KM = 1  /* transposed [K/128, ld_sa] (per group [K/128, ld_sa] when masked) */
+};
+
+/* Device error word bits (fp8bs_device_error). */
+#define FP8BS_DEVERR_TIMEOUT 0x1u       /* a pipeline wait gave up; the kernel exited early */
+#define FP8BS_DEVERR_MASKED_M 0x2u      /* masked_m[g] < 0 or > M_max (clamped) */
+#define FP8BS_DEVERR_MIXED_TILE 0x4u    /* a 128-row tile held rows of two experts */
+#define FP8BS_DEVERR_BAD_GROUP 0x8u     /* grouped_layout value >= num_groups or < -1 */
+
+/*
+ * Contiguous grouped GEMM (DeepGEMM's m_grouped_fp8_gemm_nt_contiguous
+ * contract, page section Summary).
+ *
+ *   a               E4M3 [m_sum, k]
+ *   scale_a         fp32, sa_layout FP8BS_SA_MK: [m_sum, k/128];
+ *                   FP8BS_SA_KM: [k/128, ld_sa] with ld_sa >= m_sum, ld_sa % 4 == 0
+ *   ld_sa           leading dimension of the KM layout (ignored for MK)
+ *   b               E4M3 [num_groups, n, k]
+ *   scale_b         fp32 [num_groups, n/128, k/128]
+ *   grouped_layout  int32 [m_sum]: the group of each row, -1 for a padding row.
+ *                   Each aligned 128-row tile may hold rows of at most one
+ *                   group besides -1 rows (experts padded to multiples of 128);
+ *                   other rows of a mixed tile are left unwritten and the
+ *                   device error word gets FP8BS_DEVERR_MIXED_TILE.
+ *   d               out_dtype [m_sum, n]
+ *   m_sum >= 0 (0 is a no-op), n, k > 0 multiples of 128, num_groups >= 1.
+ */
+int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, int64_t ld_sa,
+                            const void* b, const float* scale_b, const int32_t* grouped_layout,
+                            void* d, int out_dtype, int64_t m_sum, int64_t n, int64_t k,
+                            int64_t num_groups, void* stream);
+
+/*
+ * Masked grouped GEMM (DeepGEMM's m_grouped_fp8_gemm_nt_masked contract, page
+ * section Summary): group g computes only its first masked_m[g] rows.
+ *
+ *   a          E4M3 [num_groups, m_max, k]
+ *   scale_a    fp32, FP8BS_SA_MK: [num_groups, m_max, k/128];
+ *              FP8BS_SA_KM: [num_groups, k/128, ld_sa], ld_sa >= m_max, ld_sa % 4 == 0
+ *   b, scale_b as for the contiguous variant
+ *   masked_m   int32 [num_groups] in DEVICE memory, 0 <= masked_m[g] <= m_max
+ *              (values outside are clamped and flagged FP8BS_DEVERR_MASKED_M)
+ *   expected_m a hint of the typical masked_m; it never changes results (may be 0)
+ *   d          out_dtype [num_groups, m_max, n]
+ */
+int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int64_t ld_sa,
+                        const void* b, const float* scale_b, const int32_t* masked_m,
+                        int64_t expected_m, void* d, int out_dtype, int64_t num_groups,
+                        int64_t m_max, int64_t n, int64_t k, void* stream);
+
+/* Synchronises `device`, returns the FP8BS_DEVERR_* bits recorded since the
+ * last call in *flags and clears them.  Returns FP8BS_ERR_DEVICE when any bit
+ * was set, FP8BS_OK otherwise (or FP8BS_ERR_CUDA / _INVALID_ARG). */
+int fp8bs_device_error(int device, uint32_t* flags);
+
+/* Static description of an error code (never NULL). */
+const char* fp8bs_status_string(int status);
+
+/* Drops every cached TMA tensor map (host memory only).  Call after freeing
+ * tensors whose addresses may be reused with other shapes; the cache key
+ * includes address, shape and strides, so stale entries are never wrong,
+ * only kept. */
+int fp8bs_clear_cache(void);
+
+/* Library ABI version (1). */
+int fp8bs_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

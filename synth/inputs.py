@@ -187,6 +187,8 @@ class Problem:
             g, m = divmod(row, self.M_max)
             return (g, m) if m < self.group_sizes[g] else (-1, m)
         g = int(np.searchsorted(self.row_offsets, row, side="right")) - 1
+        if g >= self.G:  # the ragged tail after the last group
+            return (-1, row - self.row_offsets[-1])
         m = row - self.row_offsets[g]
         return (g, m) if m < self.group_sizes[g] else (-1, m)
 
@@ -197,6 +199,15 @@ class Problem:
         if self.variant == "contiguous":
             return self.sa[:, : self.rows].t().contiguous()
         return self.sa[:, :, : self.M_max].permute(0, 2, 1).reshape(-1, self.KB).contiguous()
+
+    def sa_mk_view(self) -> torch.Tensor:
+        """scale_a as a logical [rows, K/128] (or [G, M_max, K/128]) tensor over the stored
+        buffer: the buffer itself for SA_MK, a transposed view for SA_KM."""
+        if self.sa_layout == SA_MK:
+            return self.sa
+        if self.variant == "contiguous":
+            return self.sa[:, : self.rows].t()
+        return self.sa[:, :, : self.M_max].transpose(1, 2)
 
     def to(self, device) -> "Problem":
         mv = lambda t: None if t is None else t.to(device)  # noqa: E731

@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every
+symbol include/fp8bs.h declares, and rejects malformed arguments on the host
+before touching CUDA (every call here returns before any CUDA runtime call)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import fp8_block_scaled_gb300 as fb
+from fp8_block_scaled_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID = 0, 1
+
+
+def _declared_functions():
+    names = []
+    for fname in os.listdir(os.path.join(ROOT, "include")):
+        if not fname.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fname)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return fb.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert set(declared) == set(fb.EXPORTS), declared
+    handle = ctypes.CDLL(fb.lib_path())
+    for name in declared:
+        assert hasattr(handle, name), name
+
+
+def test_library_is_sm103a_only():
+    # the build command targets exactly compute_103a / sm_103a
+    from fp8_block_scaled_gb300 import build
+
+    assert build.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_host_only_entry_points(lib):
+    assert fb.abi_version() == 1
+    assert fb.status_string(0) == "ok"
+    assert "invalid" in fb.status_string(1)
+    assert fb.status_string(12345) == "unknown status"
+    fb.clear_cache()
+
+
+P = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+def _contig(**kw):
+    args = dict(a=P, sa=P, sa_layout=0, ld_sa=0, b=P, sb=P, lay=P, d=P, out=0,
+                m_sum=256, n=256, k=256, g=2)
+    args.update(kw)
+    return _binding.gemm_grouped_contiguous_raw(
+        args["a"], args["sa"], args["sa_layout"], args["ld_sa"], args["b"], args["sb"],
+        args["lay"], args["d"], args["out"], args["m_sum"], args["n"], args["k"], args["g"], 0)
+
+
+def _masked(**kw):
+    args = dict(a=P, sa=P, sa_layout=0, ld_sa=0, b=P, sb=P, mm=P, em=0, d=P, out=0,
+                g=2, m_max=64, n=256, k=256)
+    args.update(kw)
+    return _binding.gemm_grouped_masked_raw(
+        args["a"], args["sa"], args["sa_layout"], args["ld_sa"], args["b"], args["sb"],
+        args["mm"], args["em"], args["d"], args["out"], args["g"], args["m_max"], args["n"],
+        args["k"], 0)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(a=0), dict(sa=0), dict(b=0), dict(sb=0), dict(lay=0), dict(d=0),
+    dict(a=P + 8), dict(b=P + 4), dict(d=P + 2), dict(sa=P + 2), dict(lay=P + 1),
+    dict(n=0), dict(n=200), dict(k=100), dict(k=-128), dict(g=0), dict(m_sum=-1),
+    dict(out=2), dict(sa_layout=3),
+    dict(sa_layout=1, ld_sa=255), dict(sa_layout=1, ld_sa=258), dict(sa_layout=1, ld_sa=256, sa=P + 4),
+    dict(n=2 ** 30, g=4),
+])
+def test_contiguous_rejects(lib, bad):
+    assert _contig(**bad) == INVALID
+
+
+def test_contiguous_empty_is_noop(lib):
+    assert _contig(m_sum=0, a=0, d=0) == OK
+    assert _contig(m_sum=0, n=100) == INVALID
+
+
+@pytest.mark.parametrize("bad", [
+    dict(mm=0), dict(a=0), dict(g=0), dict(g=1025), dict(m_max=-1), dict(n=128 + 64),
+    dict(sa_layout=1, ld_sa=63), dict(sa_layout=1, ld_sa=66), dict(out=-1), dict(mm=P + 2),
+])
+def test_masked_rejects(lib, bad):
+    assert _masked(**bad) == INVALID
+
+
+def test_masked_empty_is_noop(lib):
+    assert _masked(m_max=0, a=0) == OK
+
+
+def test_scale_layout_from_strides():
+    KB = 4
+    sa_mk = torch.zeros(10, KB)
+    assert _binding._sa_layout_2d(sa_mk, 10, KB) == (fb.SA_MK, KB)
+    store = torch.zeros(KB, 12)
+    assert _binding._sa_layout_2d(store[:, :10].t(), 10, KB) == (fb.SA_KM, 12)
+    with pytest.raises(ValueError):
+        _binding._sa_layout_2d(torch.zeros(10, 2 * KB)[:, ::2], 10, KB)
+    m3 = torch.zeros(3, 5, KB)
+    assert _binding._sa_layout_3d(m3, 3, 5, KB) == (fb.SA_MK, KB)
+    s3 = torch.zeros(3, KB, 8)
+    assert _binding._sa_layout_3d(s3[:, :, :5].transpose(1, 2), 3, 5, KB) == (fb.SA_KM, 8)

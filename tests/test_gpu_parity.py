@@ -1,0 +1,188 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the CPU
+oracle on the same seeded inputs (see _parity.py for the tolerances).
+
+Small problems are compared on every row; the five named workloads at full
+size are compared on seeded samples of rows (group edges + random rows), in
+the same launch configuration bench.py times.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_gb300 as fb
+import oracle
+import synth
+from synth.inputs import OUT_BF16, OUT_F16, SA_KM, SA_MK
+
+from _parity import SENTINEL, all_rows, compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_config1_all_rows(gg):
+    p = synth.make_config("c1_contig_g2_m100_n256_k256", device=DEV)
+    bits = run_gpu(p)
+    valid, untouched = all_rows(p)
+    stats = compare(p, bits, valid, untouched)
+    assert valid.size == 200 and untouched.size == 56
+    assert stats["exact_frac"] > 0.9
+
+
+@pytest.mark.parametrize("sa_layout", [SA_MK, SA_KM])
+@pytest.mark.parametrize("out", [OUT_BF16, OUT_F16])
+def test_contiguous_ragged_multi_tile(gg, sa_layout, out):
+    """Several m/n tiles, an empty expert, an expert spanning 3 tiles, a ragged
+    M_sum tail of -1 rows, N=384 (the 128-column tile path)."""
+    p = synth.make_problem("contiguous", 3, 384, 512, [130, 0, 300], out_dtype=out,
+                           sa_layout=sa_layout, seed=31 + out, tail_rows=37, device=DEV)
+    bits = run_gpu(p)
+    valid, untouched = all_rows(p)
+    compare(p, bits, valid, untouched)
+
+
+@pytest.mark.parametrize("sa_layout", [SA_MK, SA_KM])
+def test_contiguous_wide_n_tiles(gg, sa_layout):
+    """N=768 (256-column tiles), K=1024, 4 experts of unaligned sizes."""
+    p = synth.make_problem("contiguous", 4, 768, 1024, [1, 127, 129, 256], sa_layout=sa_layout,
+                           seed=41, device=DEV)
+    bits = run_gpu(p)
+    valid, untouched = all_rows(p)
+    compare(p, bits, valid, untouched)
+
+
+@pytest.mark.parametrize("sa_layout", [SA_MK, SA_KM])
+@pytest.mark.parametrize("n", [256, 384])
+def test_masked_ragged(gg, sa_layout, n):
+    """M_max=200 (not a multiple of 128); masked_m = 0, 1, 200 (full) and 129."""
+    p = synth.make_problem("masked", 4, n, 384, [0, 1, 200, 129], M_max=200,
+                           sa_layout=sa_layout, seed=51, device=DEV)
+    bits = run_gpu(p)
+    valid, untouched = all_rows(p)
+    compare(p, bits, valid, untouched)
+
+
+def test_masked_full_equals_contiguous_bitwise(gg):
+    G, M, N, K = 3, 256, 512, 512
+    pc = synth.make_problem("contiguous", G, N, K, [M] * G, seed=61, device=DEV)
+    pm = synth.make_problem("masked", G, N, K, [M] * G, M_max=M, seed=61, device=DEV)
+    assert torch.equal(pc.a.reshape(G, M, K), pm.a) and torch.equal(pc.b, pm.b)
+    bc = run_gpu(pc)
+    bm = run_gpu(pm)
+    assert np.array_equal(bc, bm)
+
+
+def test_deterministic(gg):
+    p = synth.make_problem("contiguous", 2, 512, 768, [200, 300], seed=71, device=DEV)
+    assert np.array_equal(run_gpu(p), run_gpu(p))
+
+
+def test_empty_inputs_are_noops(gg):
+    p = synth.make_problem("masked", 3, 256, 256, [0, 0, 0], M_max=64, seed=81, device=DEV)
+    bits = run_gpu(p)
+    assert (bits == SENTINEL).all()
+    a = torch.empty((0, 256), dtype=torch.uint8, device=DEV)
+    sa = torch.empty((0, 2), dtype=torch.float32, device=DEV)
+    d = torch.empty((0, 256), dtype=torch.bfloat16, device=DEV)
+    lay = torch.empty((0,), dtype=torch.int32, device=DEV)
+    q = synth.make_problem("contiguous", 1, 256, 256, [1], seed=82, device=DEV)
+    fb.gemm_grouped_contiguous(a, sa, q.b, q.sb, d, lay)
+    torch.cuda.synchronize()
+    assert fb.device_error() == 0
+
+
+def _fill(spec, shape):
+    arr = np.empty(shape, dtype=np.uint8)
+    arr[...] = spec["default"]
+    for ranges, code in spec.get("fill", []):
+        arr[tuple(slice(lo, hi) for lo, hi in ranges)] = code
+    return arr
+
+
+with open(os.path.join(GOLDEN, "hand_cases.json")) as _f:
+    _HAND = json.load(_f)["cases"]
+
+
+@pytest.mark.parametrize("case", [c for c in _HAND if c.get("tile_aligned", True)],
+                         ids=lambda c: c["name"])
+def test_hand_cases_exact_bits(gg, case):
+    """The hand-derived golden cases: the kernel's output bits equal the
+    expected bits exactly (all of them are exact in fp32 accumulation)."""
+    K, N, G = case["K"], case["N"], case["G"]
+    b = torch.from_numpy(_fill(case["b_codes"], (G, N, K))).to(DEV)
+    sb = torch.tensor(case["scale_b"], dtype=torch.float32, device=DEV).reshape(G, N // 128, K // 128)
+    dt = torch.bfloat16 if case["out_dtype"] == 0 else torch.float16
+    if case["variant"] == "contiguous":
+        M = len(case["grouped_layout"])
+        a = torch.from_numpy(_fill(case["a_codes"], (M, K))).to(DEV)
+        sa = torch.tensor(case["scale_a"], dtype=torch.float32, device=DEV).reshape(M, K // 128)
+        lay = torch.tensor(case["grouped_layout"], dtype=torch.int32, device=DEV)
+        d = torch.full((M, N), SENTINEL, dtype=torch.int16, device=DEV).view(dt)
+        fb.gemm_grouped_contiguous(a, sa, b, sb, d, lay)
+    else:
+        Mx = case["M_max"]
+        a = torch.from_numpy(_fill(case["a_codes"], (G, Mx, K))).to(DEV)
+        sa = torch.tensor(case["scale_a"], dtype=torch.float32, device=DEV).reshape(G, Mx, K // 128)
+        mm = torch.tensor(case["masked_m"], dtype=torch.int32, device=DEV)
+        d = torch.full((G, Mx, N), SENTINEL, dtype=torch.int16, device=DEV).view(dt)
+        fb.gemm_grouped_masked(a, sa, b, sb, d, mm)
+    torch.cuda.synchronize()
+    assert fb.device_error() == 0
+    bits = d.view(torch.int16).reshape(-1, N).cpu().numpy().view(np.uint16)
+    for r, ok in enumerate(case["valid"]):
+        if not ok:
+            assert (bits[r] == SENTINEL).all()
+    for r, expect in case["expect_rows"].items():
+        for lo, hi, value, hexbits in expect["segments"]:
+            assert (bits[int(r), lo:hi] == int(hexbits, 16)).all(), (r, hex(int(bits[int(r), lo])))
+
+
+def test_device_flags_mixed_and_bad_groups(gg):
+    """A 128-row tile holding two experts, and a group id out of range, are
+    reported in the device error word.  The mixed tile is computed for its
+    highest expert id only; rows of the other expert and the out-of-range row
+    are not written."""
+    p = synth.make_problem("contiguous", 2, 256, 256, [128, 128], seed=91, device=DEV)
+    lay = p.grouped_layout.clone()
+    lay[5] = 1            # tile 0 now mixes experts 0 and 1
+    lay[200] = 7          # out of range in tile 1
+    d = torch.full((256, 256), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    fb.gemm_grouped_contiguous(p.a, p.sa, p.b, p.sb, d, lay)
+    torch.cuda.synchronize()
+    flags = fb.device_error()
+    assert flags & fb.DEVERR_MIXED_TILE and flags & fb.DEVERR_BAD_GROUP
+    bits = d.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (bits[:5] == SENTINEL).all() and (bits[6:128] == SENTINEL).all()
+    assert (bits[5] != SENTINEL).all() and (bits[200] == SENTINEL).all()
+    assert (bits[128:200] != SENTINEL).all()
+    assert fb.device_error() == 0  # cleared by the read
+
+
+def test_masked_m_out_of_range_is_clamped_and_flagged(gg):
+    p = synth.make_problem("masked", 2, 256, 256, [64, 10], M_max=64, seed=92, device=DEV)
+    mm = torch.tensor([99, 10], dtype=torch.int32, device=DEV)
+    d = torch.full((2, 64, 256), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    fb.gemm_grouped_masked(p.a, p.sa, p.b, p.sb, d, mm)
+    torch.cuda.synchronize()
+    assert fb.device_error() & fb.DEVERR_MASKED_M
+    ref = torch.full_like(d, 0).view(torch.int16).fill_(SENTINEL).view(torch.bfloat16)
+    fb.gemm_grouped_masked(p.a, p.sa, p.b, p.sb, ref, p.masked_m)  # masked_m = [64, 10]
+    torch.cuda.synchronize()
+    assert torch.equal(d.view(torch.int16), ref.view(torch.int16))
+
+
+# ------------------------------------------------------------------ the five workloads, full size
+@pytest.mark.parametrize("name", list(synth.CONFIGS))
+def test_named_workload_sampled_rows(gg, name):
+    p = synth.make_config(name, device=DEV)
+    bits = run_gpu(p)
+    if p.rows <= 4096:
+        valid, untouched = all_rows(p)
+    else:
+        valid, untouched = synth.sample_rows(p, per_group=24, seed=1)
+    stats = compare(p, bits, valid, untouched)
+    print(name, stats)

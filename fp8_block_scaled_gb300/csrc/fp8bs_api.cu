@@ -17,6 +17,7 @@
 
 #include "fp8bs.h"
 #include "grouped_gemm.cuh"
+#include "grouped_gemm_pair.cuh"
 
 // Per-device error word written by the kernels (FP8BS_DEVERR_* bits).
 __device__ uint32_t g_fp8bs_error_word;
@@ -33,7 +34,8 @@ struct DeviceState {
     int status = FP8BS_OK;      // FP8BS_ERR_UNSUPPORTED when the device is not sm_103
     int sms = 0;
     uint32_t* err = nullptr;    // device address of g_fp8bs_error_word
-    bool attr_set[16] = {};
+    bool attr_set[32] = {};
+    int max_clusters[32] = {};  // co-resident CTA pairs of each pair-kernel instantiation
 };
 
 std::mutex g_mutex;
@@ -43,10 +45,10 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 struct MapKey {
     int dev;
     const void* ptr;
-    uint64_t inner, outer, box_outer;
+    uint64_t inner, outer, box_outer, box_kb;  // box_kb = 0: 2-D map
     bool operator<(const MapKey& o) const {
-        return std::tie(dev, ptr, inner, outer, box_outer) <
-               std::tie(o.dev, o.ptr, o.inner, o.outer, o.box_outer);
+        return std::tie(dev, ptr, inner, outer, box_outer, box_kb) <
+               std::tie(o.dev, o.ptr, o.inner, o.outer, o.box_outer, o.box_kb);
     }
 };
 std::map<MapKey, CUtensorMap> g_maps;
@@ -100,7 +102,7 @@ int device_state(DeviceState** out) {
 // rows, 128-byte swizzle, out-of-range rows read as zero.
 int get_map(int dev, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer,
             const CUtensorMap** out) {
-    MapKey key{dev, ptr, inner, outer, box_outer};
+    MapKey key{dev, ptr, inner, outer, box_outer, 0};
     auto it = g_maps.find(key);
     if (it != g_maps.end()) {
         *out = &it->second;
@@ -113,6 +115,35 @@ int get_map(int dev, const void* ptr, uint64_t inner, uint64_t outer, uint32_t b
     cuuint32_t box[2] = {128u, box_outer};
     cuuint32_t estr[2] = {1u, 1u};
     CUresult r = g_encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return FP8BS_ERR_CUDA;
+    if (g_maps.size() > 4096) g_maps.clear();
+    auto ins = g_maps.emplace(key, map);
+    *out = &ins.first->second;
+    return FP8BS_OK;
+}
+
+// 3-D E4M3 tensor map over the same [outer rows, inner bytes] matrix viewed as
+// [inner/128 K blocks][outer rows][128 bytes]: a box of 128 bytes x box_outer
+// rows x box_kb K blocks lands in shared memory as box_kb consecutive
+// 128-byte-swizzled [box_outer x 128 B] tiles.
+int get_map3(int dev, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer,
+             uint32_t box_kb, const CUtensorMap** out) {
+    MapKey key{dev, ptr, inner, outer, box_outer, box_kb};
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+        *out = &it->second;
+        return FP8BS_OK;
+    }
+    CUtensorMap map;
+    std::memset(&map, 0, sizeof(map));
+    cuuint64_t dims[3] = {128u, outer, inner / 128u};
+    cuuint64_t strides[2] = {inner, 128u};  // bytes between rows, between K blocks
+    cuuint32_t box[3] = {128u, box_outer, box_kb};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -141,6 +172,60 @@ int launch(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensor
     if (grid <= 0) return FP8BS_OK;
     kern<<<grid, fp8bs::kThreads, smem, stream>>>(ta, tb, p);
     return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+// CTA-pair kernel: cluster of 2, persistent over at most the number of pairs
+// that fit on the device at once.
+template <typename OutT, bool kMasked>
+int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensorMap& tb,
+                const GemmParams& p, int64_t units_bound, cudaStream_t stream) {
+    using L = fp8bs::PairLayout;
+    auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, kMasked>;
+    const int smem = L::kBytes + L::kAlignSlack;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(fp8bs::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!st.attr_set[attr_slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        cfg.gridDim = dim3(2 * (st.sms / 2), 1, 1);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
+            cudaGetLastError();
+            clusters = st.sms / 2;
+        }
+        st.max_clusters[attr_slot] = clusters;
+        st.attr_set[attr_slot] = true;
+    }
+    const int64_t pairs = units_bound < st.max_clusters[attr_slot] ? units_bound
+                                                                   : st.max_clusters[attr_slot];
+    if (pairs <= 0) return FP8BS_OK;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_OK;
+}
+
+template <bool kMasked>
+int dispatch_pair(DeviceState& st, int out_dtype, const CUtensorMap& ta, const CUtensorMap& tb,
+                  const GemmParams& p, int64_t units_bound, cudaStream_t stream) {
+    const int slot = 16 + (kMasked ? 2 : 0) + out_dtype;
+    return out_dtype == FP8BS_OUT_BF16
+               ? launch_pair<__nv_bfloat16, kMasked>(st, slot, ta, tb, p, units_bound, stream)
+               : launch_pair<__half, kMasked>(st, slot, ta, tb, p, units_bound, stream);
 }
 
 template <bool kMasked>
@@ -225,10 +310,19 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     if (rc != FP8BS_OK) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    const int bn = pick_bn(n);
+    const int64_t m_tiles = (m_sum + 127) / 128;
+    const bool pair = n % 256 == 0 && aligned(d, 32) && m_tiles <= fp8bs::kPairMaxTiles &&
+                      num_groups < (1 << 18);
+    const int bn = pair ? 256 : pick_bn(n);
     const CUtensorMap *ta = nullptr, *tb = nullptr;
-    if ((rc = get_map(dev, a, k, m_sum, 128, &ta)) != FP8BS_OK) return rc;
-    if ((rc = get_map(dev, b, k, num_groups * n, bn, &tb)) != FP8BS_OK) return rc;
+    constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
+    if (pair) {
+        if ((rc = get_map3(dev, a, k, m_sum, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
+        if ((rc = get_map3(dev, b, k, num_groups * n, 128, kKbBox, &tb)) != FP8BS_OK) return rc;
+    } else {
+        if ((rc = get_map(dev, a, k, m_sum, 128, &ta)) != FP8BS_OK) return rc;
+        if ((rc = get_map(dev, b, k, num_groups * n, bn, &tb)) != FP8BS_OK) return rc;
+    }
 
     GemmParams p{};
     p.sa = scale_a;
@@ -249,6 +343,9 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     p.num_n_tiles = static_cast<int>(n / bn);
     p.raster_band = 8;
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+    if (pair)
+        return dispatch_pair<false>(*st, out_dtype, *ta, *tb, p, tiles,
+                                    static_cast<cudaStream_t>(stream));
     return dispatch<false>(*st, bn, out_dtype, *ta, *tb, p, tiles,
                            static_cast<cudaStream_t>(stream));
 }
@@ -279,10 +376,17 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     if (rc != FP8BS_OK) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    const int bn = pick_bn(n);
+    const bool pair = n % 256 == 0 && aligned(d, 32);
+    const int bn = pair ? 256 : pick_bn(n);
     const CUtensorMap *ta = nullptr, *tb = nullptr;
-    if ((rc = get_map(dev, a, k, num_groups * m_max, 128, &ta)) != FP8BS_OK) return rc;
-    if ((rc = get_map(dev, b, k, num_groups * n, bn, &tb)) != FP8BS_OK) return rc;
+    constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
+    if (pair) {
+        if ((rc = get_map3(dev, a, k, num_groups * m_max, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
+        if ((rc = get_map3(dev, b, k, num_groups * n, 128, kKbBox, &tb)) != FP8BS_OK) return rc;
+    } else {
+        if ((rc = get_map(dev, a, k, num_groups * m_max, 128, &ta)) != FP8BS_OK) return rc;
+        if ((rc = get_map(dev, b, k, num_groups * n, bn, &tb)) != FP8BS_OK) return rc;
+    }
 
     const int64_t kb = k / 128;
     GemmParams p{};
@@ -303,6 +407,11 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     p.num_m_tiles = static_cast<int>((m_max + 127) / 128);
     p.num_n_tiles = static_cast<int>(n / bn);
     p.raster_band = 1;
+    if (pair) {
+        const int64_t units = num_groups * ((m_max + 255) / 256) * p.num_n_tiles;
+        return dispatch_pair<true>(*st, out_dtype, *ta, *tb, p, units,
+                                   static_cast<cudaStream_t>(stream));
+    }
     const int64_t tiles = num_groups * p.num_m_tiles * p.num_n_tiles;
     return dispatch<true>(*st, bn, out_dtype, *ta, *tb, p, tiles,
                           static_cast<cudaStream_t>(stream));

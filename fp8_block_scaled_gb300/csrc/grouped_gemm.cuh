@@ -9,16 +9,20 @@
 // One CTA per SM walks a static tile list (tile = 128 rows x BN columns).
 // Warp roles inside a CTA of 256 threads:
 //   warp 0      producer: per 128-K block, TMA loads of the A tile and the B
-//               tile into a STAGES-deep shared-memory ring, plus 4-byte
-//               cp.async loads of the 128 activation scales and BN/128 weight
-//               scales of that block; all of it completes on full[stage].
-//   warp 1      MMA issuer: turns the raw fp32 scales into UE8M0 bytes laid
-//               out for tcgen05.cp, copies them to TMEM, issues four
+//               tile into a STAGES-deep shared-memory ring (complete on
+//               full[stage]), plus 4-byte cp.async loads of the 128 activation
+//               scales and BN/128 weight scales of that block (complete on
+//               sf_raw[stage]).
+//   warp 3      scale converter: turns the raw fp32 scales into UE8M0 bytes
+//               laid out for tcgen05.cp and signals sf_ready[stage].
+//   warp 1      MMA issuer: copies the stage's scales to TMEM, issues four
 //               K=32 kind::mxf8f6f4 block-scaled MMAs into the fp32 TMEM
 //               accumulator, and commits the stage back to the producer.
 //   warp 2      allocates / frees the tensor memory.
-//   warps 4-7   epilogue: TMEM -> registers -> bf16/f16 (round to nearest
-//               even) -> 16-byte stores of the rows that are valid.
+//   warps 4-7   epilogue: TMEM -> registers (64 columns per load) ->
+//               bf16/f16 (round to nearest even) -> 16-byte stores of the
+//               valid rows; the accumulator is released to the MMA warp as
+//               soon as its last columns are in registers.
 // Every mbarrier wait is bounded in time; a wait that gives up records
 // FP8BS_DEVERR_TIMEOUT, and the CTA drains its copies and MMAs, frees its
 // tensor memory and exits.
@@ -76,8 +80,8 @@ struct SmemLayout {
     static constexpr int kOffSaRaw = kOffSfb + kStages * kSfbBytes;
     static constexpr int kOffSbRaw = kOffSaRaw + kStages * kSaRawBytes;
     static constexpr int kOffBar = (kOffSbRaw + kStages * kSbRawBytes + 7) / 8 * 8;
-    // full[S], empty[S], tmem_full, tmem_empty, drain
-    static constexpr int kNumBars = 2 * kStages + 3;
+    // full[S], empty[S], sf_raw[S], sf_ready[S], tmem_full, tmem_empty, drain
+    static constexpr int kNumBars = 4 * kStages + 3;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem slot, abort flag
     static constexpr int kOffPrefix = kOffMisc + 16;
     static constexpr int kBytesContiguous = kOffPrefix;
@@ -129,10 +133,11 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
 
 // Contiguous variant: tile t -> (m_tile, n_tile) with grouped-M rasterisation
 // (bands of `raster_band` m-tiles walked column-major so that concurrently
-// running CTAs share B tiles in L2), then the tile's group from grouped_layout.
-// Warp-collective: all 32 lanes must call it with the same t.
+// running CTAs share B tiles in L2).  The first row of a 128-row tile names
+// its group (the contiguous layout pads every expert to a multiple of 128
+// rows); a tile whose first row is -1 is skipped.  Warp-uniform: every lane
+// computes the same tile.
 __device__ __forceinline__ Tile contiguous_tile(const GemmParams& p, int t, bool report) {
-    const int lane = threadIdx.x & 31;
     const int band_tiles = p.raster_band * p.num_n_tiles;
     const int band = t / band_tiles;
     const int r = t - band * band_tiles;
@@ -141,29 +146,12 @@ __device__ __forceinline__ Tile contiguous_tile(const GemmParams& p, int t, bool
     Tile tile;
     tile.m_tile = m_base + r % gm;
     tile.n_tile = r / gm;
-    int gmax = -1, gmin = 0x7fffffff;
-    bool bad = false;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int64_t row = static_cast<int64_t>(tile.m_tile) * kBM + j * 32 + lane;
-        if (row < p.rows) {
-            const int v = __ldg(p.row_info + row);
-            if (v >= p.num_groups || v < -1) {
-                bad = true;
-            } else if (v >= 0) {
-                gmax = max(gmax, v);
-                gmin = min(gmin, v);
-            }
-        }
+    int v = __ldg(p.row_info + static_cast<int64_t>(tile.m_tile) * kBM);
+    if (v >= p.num_groups || v < -1) {
+        if (report && (threadIdx.x & 31) == 0) raise_error(p.err, kErrBadGroup);
+        v = -1;
     }
-    gmax = __reduce_max_sync(0xffffffffu, gmax);
-    gmin = __reduce_min_sync(0xffffffffu, gmin);
-    bad = __any_sync(0xffffffffu, bad);
-    if (report && lane == 0) {
-        if (bad) raise_error(p.err, kErrBadGroup);
-        if (gmax >= 0 && gmin != gmax) raise_error(p.err, kErrMixedTile);
-    }
-    tile.g = gmax;
+    tile.g = v;
     return tile;
 }
 
@@ -222,9 +210,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
     auto bar_full = [&](int s) { return sbase + L::kOffBar + 8u * s; };
     auto bar_empty = [&](int s) { return sbase + L::kOffBar + 8u * (S + s); };
-    const uint32_t bar_tmem_full = sbase + L::kOffBar + 8u * (2 * S);
-    const uint32_t bar_tmem_empty = sbase + L::kOffBar + 8u * (2 * S + 1);
-    const uint32_t bar_drain = sbase + L::kOffBar + 8u * (2 * S + 2);
+    auto bar_sf_raw = [&](int s) { return sbase + L::kOffBar + 8u * (2 * S + s); };
+    auto bar_sf_ready = [&](int s) { return sbase + L::kOffBar + 8u * (3 * S + s); };
+    const uint32_t bar_tmem_full = sbase + L::kOffBar + 8u * (4 * S);
+    const uint32_t bar_tmem_empty = sbase + L::kOffBar + 8u * (4 * S + 1);
+    const uint32_t bar_drain = sbase + L::kOffBar + 8u * (4 * S + 2);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
     int* prefix = reinterpret_cast<int*>(smem + L::kOffPrefix);
@@ -232,8 +222,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ---------------------------------------------------------------- setup
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar_full(s), 1 + 32);  // producer expect_tx + 32 cp.async arrivals
+            mbar_init(bar_full(s), 1);       // producer arrive.expect_tx (+ TMA bytes)
             mbar_init(bar_empty(s), 1);      // tcgen05.commit
+            mbar_init(bar_sf_raw(s), 32);    // one cp.async arrival per producer lane
+            mbar_init(bar_sf_ready(s), 1);   // scale converter
         }
         mbar_init(bar_tmem_full, 1);
         mbar_init(bar_tmem_empty, 4);        // one arrival per epilogue warp
@@ -349,7 +341,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         p.sb + (static_cast<int64_t>(tile.g) * p.nb_count + nb0 + lane) * KB + kb;
                     cp_async_4(sbase + L::kOffSbRaw + s * L::kSbRawBytes + 4u * lane, src, 4u);
                 }
-                cp_async_mbar_arrive_noinc(bar_full(s));
+                cp_async_mbar_arrive_noinc(bar_sf_raw(s));
                 issued_mask |= 1u << s;
                 issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
                 if (++s == S) { s = 0; ph ^= 1u; }
@@ -361,7 +353,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (issued_mask & (1u << i)) {
                     const uint32_t par = (issued_parity >> i) & 1u;
                     const uint64_t t0 = global_timer_ns();
-                    while (!mbar_try_wait(bar_full(i), par) &&
+                    while (!(mbar_try_wait(bar_full(i), par) && mbar_try_wait(bar_sf_raw(i), par)) &&
                            global_timer_ns() - t0 < kWaitLimitNs) {
                     }
                 }
@@ -379,28 +371,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
             if (!warp_wait_phase(bar_tmem_empty, acc_ph ^ 1u, abort_flag, p.err)) { ok = false; break; }
             tc_fence_after();
             for (int kb = 0; kb < KB; ++kb) {
-                if (!warp_wait_phase(bar_full(s), ph, abort_flag, p.err)) { ok = false; break; }
-                tc_fence_after();
-                // scales: raw fp32 (row order) -> UE8M0 words in tcgen05.cp order:
-                // word (lane*4 + c) holds row 32*c + lane.
-                const uint32_t* raw = reinterpret_cast<const uint32_t*>(
-                    smem + L::kOffSaRaw + s * L::kSaRawBytes);
-                uint4 w;
-                w.x = ue8m0_x4(raw[lane]);
-                w.y = ue8m0_x4(raw[32 + lane]);
-                w.z = ue8m0_x4(raw[64 + lane]);
-                w.w = ue8m0_x4(raw[96 + lane]);
-                *reinterpret_cast<uint4*>(smem + L::kOffSfa + s * L::kSfaBytes + 16 * lane) = w;
-                const uint32_t* sbraw = reinterpret_cast<const uint32_t*>(
-                    smem + L::kOffSbRaw + s * L::kSbRawBytes);
-#pragma unroll
-                for (int j = 0; j < BN / 128; ++j) {
-                    const uint32_t v = ue8m0_x4(sbraw[j]);
-                    *reinterpret_cast<uint4*>(smem + L::kOffSfb + s * L::kSfbBytes + 512 * j +
-                                              16 * lane) = make_uint4(v, v, v, v);
+                if (!warp_wait_phase(bar_full(s), ph, abort_flag, p.err) ||
+                    !warp_wait_phase(bar_sf_ready(s), ph, abort_flag, p.err)) {
+                    ok = false;
+                    break;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
+                tc_fence_after();
                 if (lane == 0) {
                     const uint32_t sf_col = BN + s * L::kSfCols;
                     tc_cp_32x128b_warpx4(tmem_base + sf_col,
@@ -440,6 +416,41 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
             __syncwarp();
         }
+    } else if (warp == 3) {
+        // ============================================================ scale converter
+        // raw fp32 scales (row order) -> UE8M0 words in tcgen05.cp order:
+        // word (lane*4 + c) holds row 32*c + lane; weight scales replicated
+        // over their 128 columns.
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const Tile tile = get_tile(t, false);
+            if (tile.g < 0) continue;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!warp_wait_phase(bar_sf_raw(s), ph, abort_flag, p.err)) { ok = false; break; }
+                const uint32_t* raw = reinterpret_cast<const uint32_t*>(
+                    smem + L::kOffSaRaw + s * L::kSaRawBytes);
+                uint4 w;
+                w.x = ue8m0_x4(raw[lane]);
+                w.y = ue8m0_x4(raw[32 + lane]);
+                w.z = ue8m0_x4(raw[64 + lane]);
+                w.w = ue8m0_x4(raw[96 + lane]);
+                *reinterpret_cast<uint4*>(smem + L::kOffSfa + s * L::kSfaBytes + 16 * lane) = w;
+                const uint32_t* sbraw = reinterpret_cast<const uint32_t*>(
+                    smem + L::kOffSbRaw + s * L::kSbRawBytes);
+#pragma unroll
+                for (int j = 0; j < BN / 128; ++j) {
+                    const uint32_t v = ue8m0_x4(sbraw[j]);
+                    *reinterpret_cast<uint4*>(smem + L::kOffSfb + s * L::kSfbBytes + 512 * j +
+                                              16 * lane) = make_uint4(v, v, v, v);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_sf_ready(s));
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+        }
     } else if (warp >= 4) {
         // ============================================================ epilogue
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
@@ -459,33 +470,40 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 drow = static_cast<int64_t>(tile.g) * p.rows + m;
             } else {
                 drow = static_cast<int64_t>(tile.m_tile) * kBM + row_in_tile;
-                valid = drow < p.rows && __ldg(p.row_info + drow) == tile.g;
+                const int lv = drow < p.rows ? __ldg(p.row_info + drow) : -1;
+                valid = lv == tile.g;
+                if (!valid) {
+                    if (lv >= p.num_groups || lv < -1) raise_error(p.err, kErrBadGroup);
+                    else if (lv >= 0) raise_error(p.err, kErrMixedTile);
+                }
             }
             if (!warp_wait_phase(bar_tmem_full, acc_ph, abort_flag, p.err)) break;
             tc_fence_after();
             OutT* out = static_cast<OutT*>(p.d) + drow * p.n + tile.n_tile * BN;
+            constexpr int kChunk = 64;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tc_ld_32x32b_x32_sync(
-                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + c * 32, v);
-                uint32_t packed[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    packed[i] = pack2<OutT>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            for (int c = 0; c < BN / kChunk; ++c) {
+                uint32_t v[kChunk];
+                tc_ld_32x32b_x64_sync(
+                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + c * kChunk, v);
+                if (c == BN / kChunk - 1) {
+                    // the whole accumulator is in registers: hand TMEM back
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_tmem_empty);
                 }
                 if (valid) {
-                    uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+                    uint4* dst = reinterpret_cast<uint4*>(out + c * kChunk);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                            packed[4 * i + 3]);
+                    for (int i = 0; i < kChunk / 8; ++i) {
+                        dst[i] = make_uint4(
+                            pack2<OutT>(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
+                            pack2<OutT>(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                            pack2<OutT>(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                            pack2<OutT>(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tmem_empty);
             acc_ph ^= 1u;
         }
     }

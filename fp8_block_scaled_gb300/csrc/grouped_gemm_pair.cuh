@@ -1,0 +1,584 @@
+// CTA-pair (cluster of 2) variant of the grouped FP8 block-scaled GEMM.
+//
+// Same operation as grouped_gemm.cuh ("Adds Grouped and Batched GEMM kernels
+// with blockscaling matching DeepGEMM API", FlyDSL PR #433, section Summary),
+// computed in 256 x 256 output tiles by a pair of CTAs on two SMs: each CTA
+// holds 128 rows of A and 128 of the tile's 256 rows of B in shared memory and
+// owns a 128 x 256 fp32 accumulator in its tensor memory; the leader CTA
+// (cluster rank 0) issues tcgen05.mma.cta_group::2 with M = 256, N = 256, so
+// each SM streams 32 KB of operands per 128-K block instead of 48 KB.
+//
+// Contiguous variant: a pair of 128-row tiles must belong to one expert, so
+// the kernel first scans grouped_layout (one row per 128-row tile, the rule
+// of the contiguous layout: the first row of a tile names its expert, -1
+// skips the tile) and pairs the tiles of every expert segment two by two; an
+// odd last tile runs with the second CTA idle-storing.  Masked variant: each
+// group's first masked_m[g] rows are covered by ceil(masked_m[g] / 256) pairs.
+//
+// Operand staging: each pipeline stage holds two 128-K blocks, fetched with
+// one 3-D TMA box per operand (128 bytes x 128 rows x 2 blocks); the A and B
+// boxes are issued by two different warps.  The TMA engine completes the boxes
+// of one issuing warp one after another, so two issuers with 32 KB boxes move
+// an SM's 64 KB per stage about as fast as the MMAs consume it.
+//
+// Warp roles per CTA (both CTAs run all roles except the MMA issue):
+//   warp 0  A producer: TMA of its 128 rows of A (completion counted on the
+//           leader's full barrier, which only the leader arms, for the bytes
+//           of both CTAs), cp.async of the raw fp32 scales
+//   warp 2  B producer (after allocating the pair's tensor memory)
+//   warp 3  scale converter: UE8M0 words in tcgen05.cp order, then an
+//           arrival on the leader's full barrier of the stage
+//   warp 1  (leader only, one thread) tcgen05.cp / tcgen05.mma issue,
+//           commits multicast to both CTAs.  tcgen05.mma issue is nearly
+//           synchronous with the tensor pipe, so this thread does nothing
+//           between MMAs but one barrier wait and the scale copies.
+//   warps 4-7 epilogue of the CTA's own 128 rows
+#pragma once
+
+#include "grouped_gemm.cuh"
+
+namespace fp8bs {
+
+constexpr int kPairMaxTiles = 4096;  // contiguous: max 128-row tiles (m_sum <= 524288)
+
+struct PairLayout {
+    static constexpr int kKbPerStage = 2;                // 128-K blocks per pipeline stage
+    static constexpr int kStages = 3;
+    static constexpr int kTileBytes = 128 * kBK;         // 128 rows x one K block
+    static constexpr int kAStageBytes = kKbPerStage * kTileBytes;
+    static constexpr int kBStageBytes = kKbPerStage * kTileBytes;
+    static constexpr int kSfaBytes = 512;                // per K block
+    static constexpr int kSfbBytes = 1024;               // per K block, both 128-column chunks
+    static constexpr int kSaRawBytes = 512;              // per K block
+    static constexpr int kSbRawBytes = 16;               // per K block
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kAStageBytes;
+    static constexpr int kOffSfa = kOffB + kStages * kBStageBytes;
+    static constexpr int kOffSfb = kOffSfa + kStages * kKbPerStage * kSfaBytes;
+    static constexpr int kOffSaRaw = kOffSfb + kStages * kKbPerStage * kSfbBytes;
+    static constexpr int kOffSbRaw = kOffSaRaw + kStages * kKbPerStage * kSaRawBytes;
+    static constexpr int kOffBar =
+        (kOffSbRaw + kStages * kKbPerStage * kSbRawBytes + 7) / 8 * 8;
+    // full[S], empty[S], sf_raw[S], tmem_full, tmem_empty, drain
+    static constexpr int kNumBars = 3 * kStages + 3;
+    static constexpr int kPrefetchStages = 3;  // stages of A/B prefetched into L2 ahead of the ring
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // slot, abort, scan scratch
+    static constexpr int kMiscBytes = 16 + 2 * 8 * 4;
+    static constexpr int kOffList = (kOffMisc + kMiscBytes + 15) / 16 * 16;
+    static constexpr int kListEntries = kPairMaxTiles + 1;
+    static constexpr int kBytes = kOffList + kListEntries * 4;
+    static constexpr int kAlignSlack = 1024;
+    static constexpr int kSfColsPerKb = 4 + 8;
+    static constexpr int kTmemCols = 512;
+    static_assert(256 + kStages * kKbPerStage * kSfColsPerKb <= kTmemCols, "TMEM budget");
+    static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
+    static_assert(kPairMaxTiles * 4 <= kStages * kAStageBytes, "prologue scratch");
+};
+
+// Contiguous pair-list entry: first 128-row tile (12 bits), "second tile not
+// part of the pair" flag (bit 12), expert id (bits 13..31).
+__device__ __forceinline__ uint32_t pack_pair(int t0, bool half, int g) {
+    return static_cast<uint32_t>(t0) | (half ? 1u << 12 : 0u) | (static_cast<uint32_t>(g) << 13);
+}
+
+// Block-wide scans over one int per thread (256 threads); scratch holds 16 ints.
+__device__ __forceinline__ int block_exclusive_max(int v, int* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl = max(incl, o);
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    int prev = -1;
+    for (int w = 0; w < warp; ++w) prev = max(prev, scratch[w]);
+    const int up = __shfl_up_sync(0xffffffffu, incl, 1);
+    const int excl = lane == 0 ? prev : max(prev, up);
+    __syncthreads();
+    return excl;
+}
+
+__device__ __forceinline__ int block_exclusive_sum(int v, int* scratch, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) scratch[8 + warp] = incl;
+    __syncthreads();
+    int prev = 0, all = 0;
+    for (int w = 0; w < 8; ++w) {
+        if (w < warp) prev += scratch[8 + w];
+        all += scratch[8 + w];
+    }
+    *total = all;
+    const int excl = prev + incl - v;
+    __syncthreads();
+    return excl;
+}
+
+// Bounded wait on a local mbarrier (arrivals may come from the peer CTA, from
+// TMA completion or from tcgen05.commit).  On time-out the CTA and its peer
+// are told to abort.
+__device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t peer_abort, uint32_t* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            st_shared_cluster_u32(peer_abort, 1u);
+            raise_error(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool pair_warp_wait(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, uint32_t peer_abort,
+                                               uint32_t* err) {
+    bool ok = pair_wait(bar, parity, abort_flag, peer_abort, err);
+    return __all_sync(0xffffffffu, ok);
+}
+
+struct PairUnit {
+    int g;        // group / expert
+    int n_tile;   // 256-column tile
+    int m_base;   // first row of this CTA's half (contiguous: global row; masked: row in group)
+    bool store;   // this CTA's half belongs to the unit
+};
+
+template <typename OutT, bool kMasked>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
+    using L = PairLayout;
+    constexpr int S = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair_id = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+
+    auto bar_full = [&](int s) { return sbase + L::kOffBar + 8u * s; };
+    auto bar_empty = [&](int s) { return sbase + L::kOffBar + 8u * (S + s); };
+    auto bar_sf_raw = [&](int s) { return sbase + L::kOffBar + 8u * (2 * S + s); };
+    const uint32_t bar_tmem_full = sbase + L::kOffBar + 8u * (3 * S);
+    const uint32_t bar_tmem_empty = sbase + L::kOffBar + 8u * (3 * S + 1);
+    const uint32_t bar_drain = sbase + L::kOffBar + 8u * (3 * S + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+    int* scan_scratch = reinterpret_cast<int*>(smem + L::kOffMisc + 16);
+    int* list = reinterpret_cast<int*>(smem + L::kOffList);
+    const uint32_t peer_abort = mapa_shared(smem_addr(smem + L::kOffMisc + 4), rank ^ 1u);
+
+    // ---------------------------------------------------------------- setup
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            // leader's A and B producers (arrive.expect_tx for both CTAs' bytes) + both
+            // scale converters
+            mbar_init(bar_full(s), 4);
+            mbar_init(bar_empty(s), 1);      // leader's multicast commit
+            mbar_init(bar_sf_raw(s), 32);    // own producer lanes' cp.async arrivals
+        }
+        mbar_init(bar_tmem_full, 1);
+        mbar_init(bar_tmem_empty, 8);        // 4 epilogue warps x 2 CTAs
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_b);
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(smem_addr(tmem_slot), L::kTmemCols);
+        tmem_relinquish_pair();
+    }
+
+    int total_units;
+    if constexpr (!kMasked) {
+        // ---- pair list: tiles of each expert segment, two by two
+        const int T = p.num_m_tiles;
+        int* E = reinterpret_cast<int*>(smem + L::kOffA);  // scratch (stage buffers are idle)
+        for (int t = threadIdx.x; t < T; t += kThreads) {
+            int v = __ldg(p.row_info + static_cast<int64_t>(t) * kBM);
+            if (v >= p.num_groups || v < -1) {
+                raise_error(p.err, kErrBadGroup);
+                v = -1;
+            }
+            E[t] = v;
+        }
+        __syncthreads();
+        const int chunk = (T + kThreads - 1) / kThreads;
+        const int lo = min(T, static_cast<int>(threadIdx.x) * chunk);
+        const int hi = min(T, lo + chunk);
+        int last_start = -1;
+        for (int t = lo; t < hi; ++t)
+            if (t == 0 || E[t] != E[t - 1]) last_start = t;
+        const int carry = block_exclusive_max(last_start, scan_scratch);
+        int start = carry, count = 0;
+        for (int t = lo; t < hi; ++t) {
+            if (t == 0 || E[t] != E[t - 1]) start = t;
+            if (E[t] >= 0 && ((t - start) & 1) == 0) ++count;
+        }
+        int total = 0;
+        int idx = block_exclusive_sum(count, scan_scratch, &total);
+        start = carry;
+        for (int t = lo; t < hi; ++t) {
+            if (t == 0 || E[t] != E[t - 1]) start = t;
+            if (E[t] >= 0 && ((t - start) & 1) == 0) {
+                const bool half = (t + 1 >= T) || (E[t + 1] != E[t]);
+                list[idx++] = static_cast<int>(pack_pair(t, half, E[t]));
+            }
+        }
+        total_units = total * p.num_n_tiles;
+    } else {
+        // ---- masked: pairs per group and their prefix (warp 3)
+        if (warp == 3) {
+            const int G = p.num_groups;
+            const int per = (G + 31) / 32;
+            const int g0 = lane * per;
+            int local = 0;
+            for (int g = g0; g < min(G, g0 + per); ++g) {
+                int mm = __ldg(p.row_info + g);
+                if (mm < 0 || mm > p.rows) {
+                    raise_error(p.err, kErrMaskedM);
+                    mm = mm < 0 ? 0 : static_cast<int>(p.rows);
+                }
+                local += (mm + 2 * kBM - 1) / (2 * kBM) * p.num_n_tiles;
+            }
+            int incl = local;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            int run = incl - local;
+            for (int g = g0; g < min(G, g0 + per); ++g) {
+                list[g] = run;
+                int mm = __ldg(p.row_info + g);
+                mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
+                run += (mm + 2 * kBM - 1) / (2 * kBM) * p.num_n_tiles;
+            }
+            if (lane == 31) list[G] = incl;
+        }
+        __syncthreads();
+        total_units = list[p.num_groups];
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // peer barriers initialised, tensor memory allocated in both CTAs
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // unit u -> (group, n tile, this CTA's 128-row half)
+    auto get_unit = [&](int u) -> PairUnit {
+        PairUnit w;
+        if constexpr (!kMasked) {
+            const int P = total_units / p.num_n_tiles;
+            const int band_units = 4 * p.num_n_tiles;
+            const int band = u / band_units;
+            const int r = u - band * band_units;
+            const int gp = min(4, P - band * 4);
+            const int pi = band * 4 + r % gp;
+            w.n_tile = r / gp;
+            const uint32_t e = static_cast<uint32_t>(list[pi]);
+            const int t0 = static_cast<int>(e & 0xFFFu);
+            const bool half = (e >> 12) & 1u;
+            w.g = static_cast<int>(e >> 13);
+            w.m_base = (t0 + static_cast<int>(rank)) * kBM;
+            w.store = !(half && rank == 1);
+        } else {
+            int lo = 0, hi = p.num_groups;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (list[mid] <= u) lo = mid; else hi = mid;
+            }
+            const int local = u - list[lo];
+            const int mp = (list[lo + 1] - list[lo]) / p.num_n_tiles;
+            w.g = lo;
+            w.n_tile = local / mp;
+            w.m_base = (local - w.n_tile * mp) * 2 * kBM + static_cast<int>(rank) * kBM;
+            w.store = true;
+        }
+        return w;
+    };
+
+    constexpr uint32_t kIdesc = make_idesc_mxf8(2 * kBM, 256);
+    const int KB = p.kb_count;
+    const int NKS = (KB + L::kKbPerStage - 1) / L::kKbPerStage;  // pipeline steps per unit
+    bool aborted = false;
+
+    // First A / B row of this CTA for unit u.
+    auto unit_rows = [&](const PairUnit& w, int64_t* a_row0, int* b_row0) {
+        *a_row0 = kMasked ? static_cast<int64_t>(w.g) * p.rows + w.m_base
+                          : static_cast<int64_t>(w.m_base);
+        *b_row0 = w.g * p.n + w.n_tile * 256 + static_cast<int>(rank) * 128;
+    };
+
+    if (warp == 0 || warp == 2) {
+        // ============================================================ producers
+        // warp 0: A boxes and the raw scales; warp 2: B boxes
+        const bool is_a = warp == 0;
+        const CUtensorMap* map = is_a ? &tmap_a : &tmap_b;
+        const uint32_t op_off = is_a ? L::kOffA : L::kOffB;
+        int s = 0;
+        uint32_t ph = 0;
+        for (int u = pair_id; u < total_units && !aborted; u += num_pairs) {
+            const PairUnit w = get_unit(u);
+            int64_t a_row0;
+            int b_row0;
+            unit_rows(w, &a_row0, &b_row0);
+            const int32_t row0 = is_a ? static_cast<int32_t>(a_row0) : b_row0;
+            const int64_t sa_goff = kMasked ? static_cast<int64_t>(w.g) * p.sa_g_stride : 0;
+            const int nb0 = w.n_tile * 2;
+            for (int ks = 0; ks < NKS; ++ks) {
+                if (!pair_warp_wait(bar_empty(s), ph ^ 1u, abort_flag, peer_abort, p.err)) {
+                    aborted = true;
+                    break;
+                }
+                const int kb0 = ks * L::kKbPerStage;
+                if (lane == 0) {
+                    const uint32_t full_leader = mapa_shared(bar_full(s), 0);
+                    // the leader arms its barrier for this operand's bytes of both CTAs; the
+                    // peer's copies only complete into it
+                    if (leader) mbar_arrive_expect_tx(bar_full(s), 2u * L::kAStageBytes);
+                    tma_load_3d_pair(sbase + op_off + s * L::kAStageBytes, map, 0, row0, kb0,
+                                     full_leader);
+                    // warm L2 with the box this warp loads kPrefetchStages steps later
+                    // (the next unit's first steps near the end of this one)
+                    int kp = ks + L::kPrefetchStages;
+                    int32_t prow = row0;
+                    bool pf = true;
+                    if (kp >= NKS) {
+                        const int un = u + num_pairs;
+                        pf = un < total_units;
+                        if (pf) {
+                            int64_t na;
+                            int nbr;
+                            unit_rows(get_unit(un), &na, &nbr);
+                            prow = is_a ? static_cast<int32_t>(na) : nbr;
+                            kp -= NKS;
+                            pf = kp < NKS;
+                        }
+                    }
+                    if (pf) tma_prefetch_3d(map, 0, prow, kp * L::kKbPerStage);
+                }
+                if (is_a) {
+                    // raw scales of the stage's K blocks (zero beyond K and past the rows)
+#pragma unroll
+                    for (int j = 0; j < L::kKbPerStage; ++j) {
+                        const int kb = kb0 + j;
+                        const uint32_t sa_dst =
+                            sbase + L::kOffSaRaw + (s * L::kKbPerStage + j) * L::kSaRawBytes;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int r = q * 32 + lane;
+                            const int64_t m = static_cast<int64_t>(w.m_base) + r;
+                            const bool in = m < p.rows && kb < KB;
+                            const float* src =
+                                p.sa + sa_goff + kb * p.sa_kb_stride + m * p.sa_row_stride;
+                            cp_async_4(sa_dst + 4u * r, in ? src : p.sa, in ? 4u : 0u);
+                        }
+                        if (lane < 2) {
+                            const bool in = kb < KB;
+                            const float* src =
+                                p.sb + (static_cast<int64_t>(w.g) * p.nb_count + nb0 + lane) * KB + kb;
+                            cp_async_4(sbase + L::kOffSbRaw + (s * L::kKbPerStage + j) * L::kSbRawBytes +
+                                           4u * lane,
+                                       in ? src : p.sb, in ? 4u : 0u);
+                        }
+                    }
+                    cp_async_mbar_arrive_noinc(bar_sf_raw(s));
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer (leader)
+        if (leader && lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, acc_ph = 0;
+            bool issued_any = false;
+            for (int u = pair_id; u < total_units && !aborted; u += num_pairs) {
+                if (!pair_wait(bar_tmem_empty, acc_ph ^ 1u, abort_flag, peer_abort, p.err)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                for (int ks = 0; ks < NKS; ++ks) {
+                    if (!pair_wait(bar_full(s), ph, abort_flag, peer_abort, p.err)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < L::kKbPerStage; ++j) {
+                        const int kb = ks * L::kKbPerStage + j;
+                        if (kb >= KB) break;
+                        const int slot = s * L::kKbPerStage + j;
+                        const uint32_t sf_col = 256 + slot * L::kSfColsPerKb;
+                        tc_cp_pair_32x128b_warpx4(
+                            tmem_base + sf_col, make_desc_sf(sbase + L::kOffSfa + slot * L::kSfaBytes));
+                        tc_cp_pair_32x128b_warpx4(
+                            tmem_base + sf_col + 4,
+                            make_desc_sf(sbase + L::kOffSfb + slot * L::kSfbBytes));
+                        tc_cp_pair_32x128b_warpx4(
+                            tmem_base + sf_col + 8,
+                            make_desc_sf(sbase + L::kOffSfb + slot * L::kSfbBytes + 512));
+                        const uint64_t adesc = make_desc_sw128(sbase + L::kOffA + s * L::kAStageBytes +
+                                                               j * L::kTileBytes);
+                        const uint64_t bdesc = make_desc_sw128(sbase + L::kOffB + s * L::kBStageBytes +
+                                                               j * L::kTileBytes);
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            tc_mma_pair_mxf8(tmem_base, adesc + 2u * k, bdesc + 2u * k, kIdesc,
+                                             tmem_base + sf_col, tmem_base + sf_col + 4,
+                                             (kb | k) != 0 ? 1u : 0u);
+                        }
+                    }
+                    tc_commit_pair_mc(bar_empty(s), 0x3);
+                    issued_any = true;
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
+                if (aborted) break;
+                tc_commit_pair_mc(bar_tmem_full, 0x3);
+                acc_ph ^= 1u;
+            }
+            if (aborted && issued_any) {
+                tc_commit_pair_mc(bar_drain, 0x1);
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(bar_drain, 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ============================================================ scale converter
+        int s = 0;
+        uint32_t ph = 0;
+        for (int u = pair_id; u < total_units && !aborted; u += num_pairs) {
+            for (int ks = 0; ks < NKS; ++ks) {
+                if (!pair_warp_wait(bar_sf_raw(s), ph, abort_flag, peer_abort, p.err)) {
+                    aborted = true;
+                    break;
+                }
+#pragma unroll
+                for (int j = 0; j < L::kKbPerStage; ++j) {
+                    const int slot = s * L::kKbPerStage + j;
+                    const uint32_t* raw = reinterpret_cast<const uint32_t*>(
+                        smem + L::kOffSaRaw + slot * L::kSaRawBytes);
+                    uint4 wv;
+                    wv.x = ue8m0_x4(raw[lane]);
+                    wv.y = ue8m0_x4(raw[32 + lane]);
+                    wv.z = ue8m0_x4(raw[64 + lane]);
+                    wv.w = ue8m0_x4(raw[96 + lane]);
+                    *reinterpret_cast<uint4*>(smem + L::kOffSfa + slot * L::kSfaBytes + 16 * lane) = wv;
+                    const uint32_t* sbraw = reinterpret_cast<const uint32_t*>(
+                        smem + L::kOffSbRaw + slot * L::kSbRawBytes);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t v = ue8m0_x4(sbraw[c]);
+                        *reinterpret_cast<uint4*>(smem + L::kOffSfb + slot * L::kSfbBytes + 512 * c +
+                                                  16 * lane) = make_uint4(v, v, v, v);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(mapa_shared(bar_full(s), 0));
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+        }
+    } else if (warp >= 4) {
+        // ============================================================ epilogue
+        const int q = warp & 3;
+        const int row_in_half = q * 32 + lane;
+        const uint32_t empty_leader = mapa_shared(bar_tmem_empty, 0);
+        uint32_t acc_ph = 0;
+        for (int u = pair_id; u < total_units && !aborted; u += num_pairs) {
+            const PairUnit w = get_unit(u);
+            const int64_t m = static_cast<int64_t>(w.m_base) + row_in_half;
+            bool valid = w.store;
+            int64_t drow;
+            if constexpr (kMasked) {
+                int mm = __ldg(p.row_info + w.g);
+                mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
+                valid = valid && m < mm;
+                drow = static_cast<int64_t>(w.g) * p.rows + m;
+            } else {
+                drow = m;
+                if (valid) {
+                    const int lv = m < p.rows ? __ldg(p.row_info + m) : -1;
+                    if (lv != w.g) {
+                        if (lv >= p.num_groups || lv < -1) raise_error(p.err, kErrBadGroup);
+                        else if (lv >= 0) raise_error(p.err, kErrMixedTile);
+                        valid = false;
+                    }
+                }
+            }
+            if (!pair_warp_wait(bar_tmem_full, acc_ph, abort_flag, peer_abort, p.err)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            OutT* out = static_cast<OutT*>(p.d) + drow * p.n + w.n_tile * 256;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[64];
+                tc_ld_32x32b_x64_sync(
+                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 64, v);
+                if (c == 3) {
+                    // all TMEM reads of this tile have completed (wait::ld); the signal
+                    // publishes no memory writes, so it needs no release fence that would
+                    // wait for the global stores issued above
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
+                }
+                if (valid) {
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(out + c * 64);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        st_global_v8(dst + 32 * i,
+                                     pack2<OutT>(__uint_as_float(v[16 * i + 0]), __uint_as_float(v[16 * i + 1])),
+                                     pack2<OutT>(__uint_as_float(v[16 * i + 2]), __uint_as_float(v[16 * i + 3])),
+                                     pack2<OutT>(__uint_as_float(v[16 * i + 4]), __uint_as_float(v[16 * i + 5])),
+                                     pack2<OutT>(__uint_as_float(v[16 * i + 6]), __uint_as_float(v[16 * i + 7])),
+                                     pack2<OutT>(__uint_as_float(v[16 * i + 8]), __uint_as_float(v[16 * i + 9])),
+                                     pack2<OutT>(__uint_as_float(v[16 * i + 10]), __uint_as_float(v[16 * i + 11])),
+                                     pack2<OutT>(__uint_as_float(v[16 * i + 12]), __uint_as_float(v[16 * i + 13])),
+                                     pack2<OutT>(__uint_as_float(v[16 * i + 14]), __uint_as_float(v[16 * i + 15])));
+                    }
+                }
+            }
+            acc_ph ^= 1u;
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    if (*abort_flag) {
+        // copies issued by this CTA may still be landing in its shared memory
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 200000ull) {
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer no longer reads or signals this CTA's shared memory
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc_pair(tmem_base, L::kTmemCols);
+}
+
+}  // namespace fp8bs

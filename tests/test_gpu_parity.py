@@ -141,25 +141,50 @@ def test_hand_cases_exact_bits(gg, case):
             assert (bits[int(r), lo:hi] == int(hexbits, 16)).all(), (r, hex(int(bits[int(r), lo])))
 
 
-def test_device_flags_mixed_and_bad_groups(gg):
-    """A 128-row tile holding two experts, and a group id out of range, are
-    reported in the device error word.  The mixed tile is computed for its
-    highest expert id only; rows of the other expert and the out-of-range row
-    are not written."""
+@pytest.mark.parametrize("d_offset", [0, 8])
+def test_device_flags_mixed_and_bad_groups(gg, d_offset):
+    """The first row of a 128-row tile names its expert (the contiguous layout
+    pads every expert to a multiple of 128 rows).  A row of another expert
+    inside a tile, and a group id out of range, are reported in the device
+    error word and left unwritten.  d_offset=8 elements makes D only 16-byte
+    aligned, which selects the single-CTA kernel; 0 selects the CTA-pair kernel."""
     p = synth.make_problem("contiguous", 2, 256, 256, [128, 128], seed=91, device=DEV)
     lay = p.grouped_layout.clone()
-    lay[5] = 1            # tile 0 now mixes experts 0 and 1
-    lay[200] = 7          # out of range in tile 1
-    d = torch.full((256, 256), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    lay[5] = 1            # tile 0 (expert 0) now holds a row of expert 1
+    lay[200] = 7          # out of range in tile 1 (expert 1)
+    buf = torch.full((256 * 256 + 16,), SENTINEL, dtype=torch.int16, device=DEV)
+    d = buf[d_offset:d_offset + 256 * 256].view(torch.bfloat16).view(256, 256)
     fb.gemm_grouped_contiguous(p.a, p.sa, p.b, p.sb, d, lay)
     torch.cuda.synchronize()
     flags = fb.device_error()
     assert flags & fb.DEVERR_MIXED_TILE and flags & fb.DEVERR_BAD_GROUP
     bits = d.view(torch.int16).cpu().numpy().view(np.uint16)
-    assert (bits[:5] == SENTINEL).all() and (bits[6:128] == SENTINEL).all()
-    assert (bits[5] != SENTINEL).all() and (bits[200] == SENTINEL).all()
-    assert (bits[128:200] != SENTINEL).all()
+    assert (bits[5] == SENTINEL).all() and (bits[200] == SENTINEL).all()
+    assert (bits[:5] != SENTINEL).all() and (bits[6:200] != SENTINEL).all()
+    assert (bits[201:] != SENTINEL).all()
     assert fb.device_error() == 0  # cleared by the read
+
+
+def test_single_cta_and_pair_kernels_agree(gg):
+    """The same N%256==0 problem through both kernels (D 32-byte aligned selects
+    the CTA-pair kernel, 16-byte aligned the single-CTA kernel) against the oracle."""
+    p = synth.make_problem("contiguous", 3, 512, 768, [100, 300, 257], sa_layout=SA_KM, seed=93,
+                           device=DEV)
+    shape = (p.rows, p.N)
+    numel = p.rows * p.N
+    outs = []
+    for off in (0, 8):
+        buf = torch.full((numel + 16,), SENTINEL, dtype=torch.int16, device=DEV)
+        d = buf[off:off + numel].view(torch.bfloat16).view(*shape)
+        fb.gemm_grouped_contiguous(p.a, p.sa_mk_view(), p.b, p.sb, d, p.grouped_layout)
+        torch.cuda.synchronize()
+        assert fb.device_error() == 0
+        outs.append(d.view(torch.int16).cpu().numpy().view(np.uint16).reshape(shape))
+    valid, untouched = all_rows(p)
+    for bits in outs:
+        compare(p, bits, valid, untouched, check_fp32=False)
+    same = (outs[0] == outs[1]).mean()
+    assert same > 0.99
 
 
 def test_masked_m_out_of_range_is_clamped_and_flagged(gg):

@@ -40,13 +40,16 @@ METRIC = "grouped FP8 GEMM TFLOP/s (2*sum(m)*N*K/t)"
 FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense tensor-core ratio of GB300
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = [os.path.join(ROOT, "fp8_block_scaled_gb300", "csrc", f)
-                  for f in ("grouped_gemm.cuh", "ptx.cuh", "fp8bs_api.cu")]
+CSRC = os.path.join(ROOT, "fp8_block_scaled_gb300", "csrc")
+
+
+def _kernel_sources():
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh")))
 
 
 def kernel_hash() -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in _kernel_sources():
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -533,33 +533,33 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 break;
             }
             tc_fence_after();
-            OutT* out = static_cast<OutT*>(p.d) + drow * p.n + w.n_tile * 256;
-#pragma unroll 1
+            // the whole 256-column row goes to registers as packed bf16/f16 pairs first,
+            // so the accumulator is handed back before any global store is issued
+            uint32_t packed[4][32];
+#pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[64];
                 tc_ld_32x32b_x64_sync(
                     tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 64, v);
-                if (c == 3) {
-                    // all TMEM reads of this tile have completed (wait::ld); the signal
-                    // publishes no memory writes, so it needs no release fence that would
-                    // wait for the global stores issued above
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
-                }
-                if (valid) {
-                    uint8_t* dst = reinterpret_cast<uint8_t*>(out + c * 64);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    packed[c][i] = pack2<OutT>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            }
+            // all TMEM reads of this tile have completed (wait::ld); the signal publishes
+            // no memory writes, so it is a relaxed arrival
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
+            if (valid) {
+                uint8_t* dst = reinterpret_cast<uint8_t*>(static_cast<OutT*>(p.d) + drow * p.n +
+                                                          w.n_tile * 256);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        st_global_v8(dst + 32 * i,
-                                     pack2<OutT>(__uint_as_float(v[16 * i + 0]), __uint_as_float(v[16 * i + 1])),
-                                     pack2<OutT>(__uint_as_float(v[16 * i + 2]), __uint_as_float(v[16 * i + 3])),
-                                     pack2<OutT>(__uint_as_float(v[16 * i + 4]), __uint_as_float(v[16 * i + 5])),
-                                     pack2<OutT>(__uint_as_float(v[16 * i + 6]), __uint_as_float(v[16 * i + 7])),
-                                     pack2<OutT>(__uint_as_float(v[16 * i + 8]), __uint_as_float(v[16 * i + 9])),
-                                     pack2<OutT>(__uint_as_float(v[16 * i + 10]), __uint_as_float(v[16 * i + 11])),
-                                     pack2<OutT>(__uint_as_float(v[16 * i + 12]), __uint_as_float(v[16 * i + 13])),
-                                     pack2<OutT>(__uint_as_float(v[16 * i + 14]), __uint_as_float(v[16 * i + 15])));
+                        st_global_v8(dst + 128 * c + 32 * i, packed[c][8 * i], packed[c][8 * i + 1],
+                                     packed[c][8 * i + 2], packed[c][8 * i + 3], packed[c][8 * i + 4],
+                                     packed[c][8 * i + 5], packed[c][8 * i + 6], packed[c][8 * i + 7]);
                     }
                 }
             }

@@ -53,6 +53,50 @@ struct MapKey {
 };
 std::map<MapKey, CUtensorMap> g_maps;
 
+// Stream-K scratch of the CTA-pair kernel, one per (device, stream): launches on
+// one stream run one after another, so they may share it; launches on different
+// streams may overlap and must not.
+struct SkWorkspace {
+    float* partial = nullptr;
+    uint32_t* flags = nullptr;
+    int slots = 0;
+};
+std::map<std::pair<int, void*>, SkWorkspace> g_sk;
+constexpr size_t kSkSlotBytes = 128 * 256 * sizeof(float);
+
+// Returns the stream's workspace with at least `slots` slots, allocating it on
+// first use; nullptr (stream-K off for this launch) when that would need an
+// allocation while the stream is being captured, or when allocation fails.
+SkWorkspace* sk_workspace(int dev, cudaStream_t stream, int slots) {
+    auto key = std::make_pair(dev, static_cast<void*>(stream));
+    auto it = g_sk.find(key);
+    if (it != g_sk.end() && it->second.slots >= slots) return &it->second;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (it != g_sk.end()) {
+        cudaStreamSynchronize(stream);
+        cudaFree(it->second.partial);
+        cudaFree(it->second.flags);
+        g_sk.erase(it);
+    }
+    SkWorkspace w;
+    if (cudaMalloc(&w.partial, kSkSlotBytes * slots) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cudaMalloc(&w.flags, 2 * sizeof(uint32_t) * slots) != cudaSuccess ||
+        cudaMemsetAsync(w.flags, 0, 2 * sizeof(uint32_t) * slots, stream) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(w.partial);
+        return nullptr;
+    }
+    w.slots = slots;
+    return &(g_sk[key] = w);
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Resolve the current device and its cached state (lock held by caller).
@@ -211,8 +255,17 @@ int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUt
     const int64_t pairs = units_bound < st.max_clusters[attr_slot] ? units_bound
                                                                    : st.max_clusters[attr_slot];
     if (pairs <= 0) return FP8BS_OK;
+    GemmParams q = p;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    SkWorkspace* w = kMasked ? nullptr : sk_workspace(dev, stream, 2 * st.max_clusters[attr_slot]);
+    if (w != nullptr) {
+        q.sk_partial = w->partial;
+        q.sk_flags = w->flags;
+        q.sk_slots = w->slots;
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, q) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
@@ -222,6 +275,9 @@ int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUt
 template <bool kMasked>
 int dispatch_pair(DeviceState& st, int out_dtype, const CUtensorMap& ta, const CUtensorMap& tb,
                   const GemmParams& p, int64_t units_bound, cudaStream_t stream) {
+    // The masked (decode) variant streams each B tile once for all the m-tiles of its
+    // group; splitting units across pairs would fetch it again later, so it stays
+    // round-robin and needs no scratch.
     const int slot = 16 + (kMasked ? 2 : 0) + out_dtype;
     return out_dtype == FP8BS_OUT_BF16
                ? launch_pair<__nv_bfloat16, kMasked>(st, slot, ta, tb, p, units_bound, stream)
@@ -433,6 +489,13 @@ int fp8bs_device_error(int device, uint32_t* flags) {
         cudaMemcpyToSymbol(g_fp8bs_error_word, &zero, sizeof(zero)) != cudaSuccess) {
         cudaGetLastError();
         rc = FP8BS_ERR_CUDA;
+    }
+    if (rc == FP8BS_OK && value != 0) {
+        // a launch that gave up may have left stream-K slot counters half set
+        for (auto& kv : g_sk)
+            if (kv.first.first == device) cudaMemset(kv.second.flags, 0, 2 * sizeof(uint32_t) * kv.second.slots);
+        cudaDeviceSynchronize();
+        cudaGetLastError();
     }
     cudaSetDevice(old);
     *flags = value;

@@ -62,6 +62,10 @@ struct GemmParams {
     int num_m_tiles;             // contiguous: ceil(m_sum/128); masked: ceil(m_max/128)
     int num_n_tiles;
     int raster_band;             // contiguous: m-tiles per rasterisation band
+    // stream-K tail of the CTA-pair kernel (sk_slots == 0 disables it)
+    float* sk_partial;           // sk_slots x [128 rows x 256 cols] fp32 partial accumulators
+    uint32_t* sk_flags;          // 2 words per slot (ready warps, consumed warps), 0 between launches
+    int sk_slots;                // slots available (needs 2 per CTA pair of the grid)
 };
 
 template <int BN>

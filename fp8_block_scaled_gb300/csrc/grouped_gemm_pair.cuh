@@ -15,6 +15,18 @@
 // odd last tile runs with the second CTA idle-storing.  Masked variant: each
 // group's first masked_m[g] rows are covered by ceil(masked_m[g] / 256) pairs.
 //
+// Scheduling: units (one 256 x 256 tile each) go round-robin to the pairs of
+// the persistent grid.  When the unit count is not a multiple of the pair
+// count, the units of the last two rounds are instead cut into equal runs of
+// K steps, one contiguous run per pair (stream-K): every unit is then split at
+// most once, into a head [0, x) finished last by one pair and a tail [x, end)
+// finished first by the next pair.  Each epilogue warp of the tail writes its
+// rows of the fp32 partial accumulator to a scratch slot and counts itself in
+// the slot's ready word; each epilogue warp of the head waits (bounded) until
+// all four have, adds the partial, and the last of them resets the slot's
+// words to zero for the next launch.  No warp waits on another warp of its
+// own CTA, so a warp that aborts cannot block the others.
+//
 // Operand staging: each pipeline stage holds two 128-K blocks, fetched with
 // one 3-D TMA box per operand (128 bytes x 128 rows x 2 blocks); the A and B
 // boxes are issued by two different warps.  The TMA engine completes the boxes
@@ -146,6 +158,13 @@ __device__ __forceinline__ bool pair_warp_wait(uint32_t bar, uint32_t parity,
     bool ok = pair_wait(bar, parity, abort_flag, peer_abort, err);
     return __all_sync(0xffffffffu, ok);
 }
+
+// One run of K steps [ks0, ks1) of unit u executed by a pair.
+struct PairPiece {
+    int u;      // < 0: no more pieces
+    int ks0, ks1;
+    int kind;   // 0 whole unit, 1 head (adds the partial of the unit's tail), 2 tail
+};
 
 struct PairUnit {
     int g;        // group / expert
@@ -321,6 +340,54 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int NKS = (KB + L::kKbPerStage - 1) / L::kKbPerStage;  // pipeline steps per unit
     bool aborted = false;
 
+    // ---- schedule: round-robin units, then a stream-K tail (same on every thread)
+    // Worth it when the idle share of the last round, spread over all rounds, is
+    // above 10% (the partial tiles cost a few microseconds); the masked variant
+    // (launched with sk_slots = 0) keeps the m-tiles of one B tile together.
+    const int last_round = total_units % num_pairs;
+    const int rounds = (total_units + num_pairs - 1) / num_pairs;
+    const bool use_sk = p.sk_slots >= 2 * num_pairs && total_units > num_pairs && last_round != 0 &&
+                        (num_pairs - last_round) * 10 > num_pairs * rounds;
+    int dp_count, dp_units = 0, sk_begin = 0, sk_end = 0;
+    if (use_sk) {
+        dp_count = total_units / num_pairs - 1;
+        dp_units = dp_count * num_pairs;
+        const int64_t work = static_cast<int64_t>(total_units - dp_units) * NKS;
+        sk_begin = static_cast<int>(work * pair_id / num_pairs);
+        sk_end = static_cast<int>(work * (pair_id + 1) / num_pairs);
+    } else {
+        dp_count = pair_id < total_units ? (total_units - pair_id + num_pairs - 1) / num_pairs : 0;
+    }
+    auto get_piece = [&](int i) -> PairPiece {
+        PairPiece pc;
+        pc.u = -1;
+        pc.ks0 = 0;
+        pc.ks1 = NKS;
+        pc.kind = 0;
+        if (i < dp_count) {
+            pc.u = pair_id + i * num_pairs;
+            return pc;
+        }
+        if (!use_sk) return pc;
+        int j = i - dp_count;
+        int pos = sk_begin;
+        while (pos < sk_end) {
+            const int uu = pos / NKS;
+            const int k0 = pos - uu * NKS;
+            const int k1 = min(NKS, k0 + (sk_end - pos));
+            if (j == 0) {
+                pc.u = dp_units + uu;
+                pc.ks0 = k0;
+                pc.ks1 = k1;
+                pc.kind = k0 > 0 ? 2 : (k1 < NKS ? 1 : 0);
+                return pc;
+            }
+            --j;
+            pos += k1 - k0;
+        }
+        return pc;
+    };
+
     // First A / B row of this CTA for unit u.
     auto unit_rows = [&](const PairUnit& w, int64_t* a_row0, int* b_row0) {
         *a_row0 = kMasked ? static_cast<int64_t>(w.g) * p.rows + w.m_base
@@ -336,15 +403,17 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint32_t op_off = is_a ? L::kOffA : L::kOffB;
         int s = 0;
         uint32_t ph = 0;
-        for (int u = pair_id; u < total_units && !aborted; u += num_pairs) {
-            const PairUnit w = get_unit(u);
+        for (int pi = 0; !aborted; ++pi) {
+            const PairPiece pc = get_piece(pi);
+            if (pc.u < 0) break;
+            const PairUnit w = get_unit(pc.u);
             int64_t a_row0;
             int b_row0;
             unit_rows(w, &a_row0, &b_row0);
             const int32_t row0 = is_a ? static_cast<int32_t>(a_row0) : b_row0;
             const int64_t sa_goff = kMasked ? static_cast<int64_t>(w.g) * p.sa_g_stride : 0;
             const int nb0 = w.n_tile * 2;
-            for (int ks = 0; ks < NKS; ++ks) {
+            for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
                 if (!pair_warp_wait(bar_empty(s), ph ^ 1u, abort_flag, peer_abort, p.err)) {
                     aborted = true;
                     break;
@@ -358,20 +427,20 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tma_load_3d_pair(sbase + op_off + s * L::kAStageBytes, map, 0, row0, kb0,
                                      full_leader);
                     // warm L2 with the box this warp loads kPrefetchStages steps later
-                    // (the next unit's first steps near the end of this one)
+                    // (the next piece's first steps near the end of this one)
                     int kp = ks + L::kPrefetchStages;
                     int32_t prow = row0;
                     bool pf = true;
-                    if (kp >= NKS) {
-                        const int un = u + num_pairs;
-                        pf = un < total_units;
+                    if (kp >= pc.ks1) {
+                        const PairPiece np = get_piece(pi + 1);
+                        pf = np.u >= 0;
                         if (pf) {
                             int64_t na;
                             int nbr;
-                            unit_rows(get_unit(un), &na, &nbr);
+                            unit_rows(get_unit(np.u), &na, &nbr);
                             prow = is_a ? static_cast<int32_t>(na) : nbr;
-                            kp -= NKS;
-                            pf = kp < NKS;
+                            kp = np.ks0 + (kp - pc.ks1);
+                            pf = kp < np.ks1;
                         }
                     }
                     if (pf) tma_prefetch_3d(map, 0, prow, kp * L::kKbPerStage);
@@ -412,13 +481,15 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             int s = 0;
             uint32_t ph = 0, acc_ph = 0;
             bool issued_any = false;
-            for (int u = pair_id; u < total_units && !aborted; u += num_pairs) {
+            for (int pi = 0; !aborted; ++pi) {
+                const PairPiece pc = get_piece(pi);
+                if (pc.u < 0) break;
                 if (!pair_wait(bar_tmem_empty, acc_ph ^ 1u, abort_flag, peer_abort, p.err)) {
                     aborted = true;
                     break;
                 }
                 tc_fence_after();
-                for (int ks = 0; ks < NKS; ++ks) {
+                for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
                     if (!pair_wait(bar_full(s), ph, abort_flag, peer_abort, p.err)) {
                         aborted = true;
                         break;
@@ -444,9 +515,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                                j * L::kTileBytes);
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            // the first MMA of a piece overwrites the accumulator
                             tc_mma_pair_mxf8(tmem_base, adesc + 2u * k, bdesc + 2u * k, kIdesc,
                                              tmem_base + sf_col, tmem_base + sf_col + 4,
-                                             (kb | k) != 0 ? 1u : 0u);
+                                             (ks > pc.ks0 || j > 0 || k > 0) ? 1u : 0u);
                         }
                     }
                     tc_commit_pair_mc(bar_empty(s), 0x3);
@@ -469,8 +541,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         // ============================================================ scale converter
         int s = 0;
         uint32_t ph = 0;
-        for (int u = pair_id; u < total_units && !aborted; u += num_pairs) {
-            for (int ks = 0; ks < NKS; ++ks) {
+        for (int pi = 0; !aborted; ++pi) {
+            const PairPiece pc = get_piece(pi);
+            if (pc.u < 0) break;
+            for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
                 if (!pair_warp_wait(bar_sf_raw(s), ph, abort_flag, peer_abort, p.err)) {
                     aborted = true;
                     break;
@@ -507,8 +581,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const int row_in_half = q * 32 + lane;
         const uint32_t empty_leader = mapa_shared(bar_tmem_empty, 0);
         uint32_t acc_ph = 0;
-        for (int u = pair_id; u < total_units && !aborted; u += num_pairs) {
-            const PairUnit w = get_unit(u);
+        for (int pi = 0; !aborted; ++pi) {
+            const PairPiece pc = get_piece(pi);
+            if (pc.u < 0) break;
+            const PairUnit w = get_unit(pc.u);
             const int64_t m = static_cast<int64_t>(w.m_base) + row_in_half;
             bool valid = w.store;
             int64_t drow;
@@ -533,33 +609,119 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 break;
             }
             tc_fence_after();
-            // the whole 256-column row goes to registers as packed bf16/f16 pairs first,
-            // so the accumulator is handed back before any global store is issued
-            uint32_t packed[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[64];
-                tc_ld_32x32b_x64_sync(
-                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 64, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    packed[c][i] = pack2<OutT>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            }
-            // all TMEM reads of this tile have completed (wait::ld); the signal publishes
-            // no memory writes, so it is a relaxed arrival
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
-            if (valid) {
-                uint8_t* dst = reinterpret_cast<uint8_t*>(static_cast<OutT*>(p.d) + drow * p.n +
-                                                          w.n_tile * 256);
+            const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            uint8_t* dst = reinterpret_cast<uint8_t*>(static_cast<OutT*>(p.d) + drow * p.n +
+                                                      w.n_tile * 256);
+            if (pc.kind == 0) {
+                // the whole 256-column row goes to registers as packed bf16/f16 pairs
+                // first, so the accumulator is handed back before any global store
+                uint32_t packed[4][32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
+                    uint32_t v[64];
+                    tc_ld_32x32b_x64_sync(trow + c * 64, v);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        st_global_v8(dst + 128 * c + 32 * i, packed[c][8 * i], packed[c][8 * i + 1],
-                                     packed[c][8 * i + 2], packed[c][8 * i + 3], packed[c][8 * i + 4],
-                                     packed[c][8 * i + 5], packed[c][8 * i + 6], packed[c][8 * i + 7]);
+                    for (int i = 0; i < 32; ++i)
+                        packed[c][i] =
+                            pack2<OutT>(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                }
+                // all TMEM reads of this tile have completed (wait::ld); the signal
+                // publishes no memory writes, so it is a relaxed arrival
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            st_global_v8(dst + 128 * c + 32 * i, packed[c][8 * i],
+                                         packed[c][8 * i + 1], packed[c][8 * i + 2],
+                                         packed[c][8 * i + 3], packed[c][8 * i + 4],
+                                         packed[c][8 * i + 5], packed[c][8 * i + 6],
+                                         packed[c][8 * i + 7]);
+                        }
+                    }
+                }
+            } else if (pc.kind == 2) {
+                // tail: publish the fp32 partial of this CTA's 128 rows in slot
+                // (pair, rank), laid out [32 column groups][128 rows][8 columns] so that
+                // each warp store covers 1 KB of contiguous memory; each warp then
+                // counts itself in the slot's ready word
+                const int slot = pair_id * 2 + static_cast<int>(rank);
+                float* part = p.sk_partial + static_cast<int64_t>(slot) * (128 * 256) + row_in_half * 8;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[64];
+                    tc_ld_32x32b_x64_sync(trow + c * 64, v);
+                    if (c == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        st_global_v8(part + (c * 8 + i) * (128 * 8), v[8 * i], v[8 * i + 1],
+                                     v[8 * i + 2], v[8 * i + 3], v[8 * i + 4], v[8 * i + 5],
+                                     v[8 * i + 6], v[8 * i + 7]);
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(p.sk_flags + 2 * slot, 1u);
+            } else {
+                // head: wait until the four tail warps of the same unit (the next pair's
+                // first piece) have published their rows, add the partial, store
+                const int slot = (pair_id + 1) * 2 + static_cast<int>(rank);
+                if (lane == 0) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (ld_acquire_gpu_u32(p.sk_flags + 2 * slot) < 4u) {
+                        if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+                            raise_error(p.err, kErrTimeout);
+                            break;
+                        }
+                    }
+                }
+                __syncwarp();
+                const float* part =
+                    p.sk_partial + static_cast<int64_t>(slot) * (128 * 256) + row_in_half * 8;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[64];
+                    tc_ld_32x32b_x64_sync(trow + c * 64, v);
+                    if (c == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
+                    }
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        // L2-only loads: this SM may hold stale L1 lines of the slot from an
+                        // earlier launch
+                        const float4 f = __ldcg(reinterpret_cast<const float4*>(
+                            part + (c * 8 + i / 2) * (128 * 8) + 4 * (i & 1)));
+                        pk[2 * i] = pack2<OutT>(__uint_as_float(v[4 * i]) + f.x,
+                                                __uint_as_float(v[4 * i + 1]) + f.y);
+                        pk[2 * i + 1] = pack2<OutT>(__uint_as_float(v[4 * i + 2]) + f.z,
+                                                    __uint_as_float(v[4 * i + 3]) + f.w);
+                    }
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            st_global_v8(dst + 128 * c + 32 * i, pk[8 * i], pk[8 * i + 1],
+                                         pk[8 * i + 2], pk[8 * i + 3], pk[8 * i + 4], pk[8 * i + 5],
+                                         pk[8 * i + 6], pk[8 * i + 7]);
+                        }
+                    }
+                }
+                // the last of the four head warps to finish reading resets the slot
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    if (atomicAdd(p.sk_flags + 2 * slot + 1, 1u) == 3u) {
+                        p.sk_flags[2 * slot] = 0u;
+                        p.sk_flags[2 * slot + 1] = 0u;
                     }
                 }
             }

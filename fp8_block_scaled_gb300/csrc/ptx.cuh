@@ -312,6 +312,12 @@ __device__ __forceinline__ void tc_mma_pair_mxf8(uint32_t d_tmem, uint64_t a_des
         : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* ptr) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 // 32-byte global store (sm_100+ 256-bit vector store).
 __device__ __forceinline__ void st_global_v8(void* ptr, uint32_t a0, uint32_t a1, uint32_t a2,
                                              uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,

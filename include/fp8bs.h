@@ -27,8 +27,16 @@
  *    for the transposed activation-scale layout, whose ld_sa must be a
  *    multiple of 4).  N and K must be positive multiples of 128.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
- *    asynchronous: they validate, enqueue one kernel and return.  Nothing is
- *    allocated on the device.
+ *    asynchronous: they validate, enqueue one kernel and return.
+ *  - Scratch: the CTA-pair kernel balances its last rounds with a stream-K
+ *    split whose fp32 partial tiles live in a per-(device, stream) workspace
+ *    (about 20 MB on a 152-SM GB300) that the library allocates with
+ *    cudaMalloc on the first such call on that stream and keeps until exit.
+ *    If that first call happens while the stream is being captured into a
+ *    CUDA graph, or the allocation fails, the call runs without the split
+ *    (same results, less balanced).  Launches on one stream share the
+ *    workspace safely; concurrent launches on different streams use
+ *    different workspaces.
  *  - Rows that are not computed (grouped_layout == -1, or m >= masked_m[g])
  *    are not written: D keeps its prior contents there.
  *  - Return value: FP8BS_OK, or an error code; nothing is enqueued on error.
@@ -79,10 +87,12 @@ enum fp8bs_sa_layout {
  *   b               E4M3 [num_groups, n, k]
  *   scale_b         fp32 [num_groups, n/128, k/128]
  *   grouped_layout  int32 [m_sum]: the group of each row, -1 for a padding row.
- *                   Each aligned 128-row tile may hold rows of at most one
- *                   group besides -1 rows (experts padded to multiples of 128);
- *                   other rows of a mixed tile are left unwritten and the
- *                   device error word gets FP8BS_DEVERR_MIXED_TILE.
+ *                   Experts are padded to multiples of 128 rows: the first
+ *                   row of each aligned 128-row tile names the tile's group
+ *                   (-1 there skips the whole tile).  Rows of another group
+ *                   inside a tile are left unwritten and set
+ *                   FP8BS_DEVERR_MIXED_TILE; ids outside [-1, num_groups) set
+ *                   FP8BS_DEVERR_BAD_GROUP.
  *   d               out_dtype [m_sum, n]
  *   m_sum >= 0 (0 is a no-op), n, k > 0 multiples of 128, num_groups >= 1.
  */

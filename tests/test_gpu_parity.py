@@ -200,6 +200,37 @@ def test_masked_m_out_of_range_is_clamped_and_flagged(gg):
     assert torch.equal(d.view(torch.int16), ref.view(torch.int16))
 
 
+# ------------------------------------------------------------------ stream-K tail of the pair kernel
+# 80 units of 256 x 256 on a 152-SM GB300 (76 CTA pairs) are not a multiple of
+# the pair count, so the units are cut into K runs split across pairs.
+def test_stream_k_contiguous_all_rows_and_repeat(gg):
+    p = synth.make_problem("contiguous", 2, 2560, 1024, [1024, 1000], sa_layout=SA_KM, seed=101,
+                           device=DEV)
+    bits1 = run_gpu(p)
+    valid, untouched = all_rows(p)
+    compare(p, bits1, valid, untouched, check_fp32=False)
+    bits2 = run_gpu(p)  # slot counters were reset by the first launch
+    assert np.array_equal(bits1, bits2)
+
+
+def test_masked_many_units_all_rows(gg):
+    """Masked problems always run round-robin (no stream-K split); 80 units."""
+    p = synth.make_problem("masked", 4, 2560, 768, [512, 300, 512, 257], M_max=512, seed=102,
+                           device=DEV)
+    bits = run_gpu(p)
+    valid, untouched = all_rows(p)
+    compare(p, bits, valid, untouched, check_fp32=False)
+
+
+def test_stream_k_on_a_second_stream(gg):
+    p = synth.make_problem("contiguous", 2, 2560, 1024, [1024, 1000], seed=103, device=DEV)
+    ref = run_gpu(p)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        bits = run_gpu(p, stream=side)
+    assert np.array_equal(ref, bits)
+
+
 # ------------------------------------------------------------------ the five workloads, full size
 @pytest.mark.parametrize("name", list(synth.CONFIGS))
 def test_named_workload_sampled_rows(gg, name):

@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     clear_cache,
     device_error,
     gemm_grouped_contiguous,
+    gemm_grouped_contiguous_noalloc_raw,
     gemm_grouped_contiguous_raw,
     gemm_grouped_masked,
     gemm_grouped_masked_raw,

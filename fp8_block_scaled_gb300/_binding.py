@@ -28,8 +28,8 @@ DEVERR_MIXED_TILE = 0x4
 DEVERR_BAD_GROUP = 0x8
 
 # every symbol include/fp8bs.h declares
-EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "fp8bs_device_error",
-           "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version")
+EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "gemm_grouped_contiguous_noalloc",
+           "fp8bs_device_error", "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version")
 
 _lib = None
 _lock = threading.Lock()
@@ -65,6 +65,9 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.gemm_grouped_masked.argtypes = [_P, _P, _I, _I64, _P, _P, _P, _I64, _P, _I,
                                             _I64, _I64, _I64, _I64, _P]
         lib.gemm_grouped_masked.restype = _I
+        lib.gemm_grouped_contiguous_noalloc.argtypes = [_P, _P, _I, _I64, _P, _P, _P, _P, _I,
+                                                        _I64, _I64, _I64, _I64, _P]
+        lib.gemm_grouped_contiguous_noalloc.restype = _I
         lib.fp8bs_device_error.argtypes = [_I, ctypes.POINTER(ctypes.c_uint32)]
         lib.fp8bs_device_error.restype = _I
         lib.fp8bs_status_string.argtypes = [_I]
@@ -141,6 +144,17 @@ def gemm_grouped_contiguous_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr, 
     return lib.gemm_grouped_contiguous(a_ptr, sa_ptr, int(sa_layout), int(ld_sa), b_ptr, sb_ptr,
                                        layout_ptr, d_ptr, int(out_dtype), int(m_sum), int(n),
                                        int(k), int(num_groups), ctypes.c_void_p(_stream_handle(stream)))
+
+
+def gemm_grouped_contiguous_noalloc_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr,
+                                        layout_ptr, d_ptr, out_dtype, m_sum, n, k, num_groups,
+                                        stream=None) -> int:
+    """C-ABI call of the variant that allocates no device memory (raw pointers)."""
+    lib = load()
+    return lib.gemm_grouped_contiguous_noalloc(
+        a_ptr, sa_ptr, int(sa_layout), int(ld_sa), b_ptr, sb_ptr, layout_ptr, d_ptr,
+        int(out_dtype), int(m_sum), int(n), int(k), int(num_groups),
+        ctypes.c_void_p(_stream_handle(stream)))
 
 
 def gemm_grouped_masked_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr, masked_m_ptr,

@@ -321,6 +321,98 @@ int pick_bn(int64_t n) { return n % 256 == 0 ? 256 : 128; }
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Scratch of gemm_grouped_contiguous_noalloc: the stream-K partial tiles and
+// slot counters of the CTA-pair kernel in one statically sized device array,
+// for callers that may not allocate device memory.  Every GPU that loads this
+// library holds it until the process exits.
+namespace {
+constexpr int kNoAllocSlots = 160;  // 2 per CTA pair, up to 80 pairs
+constexpr size_t kNoAllocPartialBytes = kNoAllocSlots * kSkSlotBytes;
+constexpr size_t kNoAllocFlagBytes = 2 * sizeof(uint32_t) * kNoAllocSlots;
+}  // namespace
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocPartialBytes + kNoAllocFlagBytes];
+
+namespace {
+
+struct NoAllocDevice {
+    bool ready = false;
+    unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
+    bool attr_set[2] = {};
+    int max_clusters[2] = {};
+};
+NoAllocDevice g_noalloc[kMaxDevices];
+
+// 2-D/3-D maps are encoded on the stack for every call (no cache, no host heap).
+int encode_map3_noalloc(const void* ptr, uint64_t inner, uint64_t outer, CUtensorMap* map) {
+    std::memset(map, 0, sizeof(*map));
+    cuuint64_t dims[3] = {128u, outer, inner / 128u};
+    cuuint64_t strides[2] = {inner, 128u};
+    cuuint32_t box[3] = {128u, 128u, static_cast<cuuint32_t>(fp8bs::PairLayout::kKbPerStage)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+template <typename OutT>
+int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUtensorMap& ta,
+                        const CUtensorMap& tb, GemmParams q, int64_t units_bound,
+                        cudaStream_t stream) {
+    using L = fp8bs::PairLayout;
+    auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, false>;
+    const int smem = L::kBytes + L::kAlignSlack;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(fp8bs::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!nd.attr_set[slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        cfg.gridDim = dim3(2 * (st.sms / 2), 1, 1);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
+            cudaGetLastError();
+            clusters = st.sms / 2;
+        }
+        nd.max_clusters[slot] = clusters;
+        nd.attr_set[slot] = true;
+    }
+    const int64_t pairs = units_bound < nd.max_clusters[slot] ? units_bound : nd.max_clusters[slot];
+    if (pairs <= 0) return FP8BS_OK;
+    if (2 * pairs > kNoAllocSlots) return FP8BS_ERR_INVALID_ARG;  // more pairs than the array holds
+    // the slot counters must start at zero; a launch that gave up could have left
+    // them set, so clear them on the stream before every launch
+    uint32_t* flags = reinterpret_cast<uint32_t*>(nd.scratch + kNoAllocPartialBytes);
+    if (cudaMemsetAsync(flags, 0, kNoAllocFlagBytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    q.sk_partial = reinterpret_cast<float*>(nd.scratch);
+    q.sk_flags = flags;
+    q.sk_slots = kNoAllocSlots;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, q) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int fp8bs_abi_version(void) { return 1; }
@@ -471,6 +563,76 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     const int64_t tiles = num_groups * p.num_m_tiles * p.num_n_tiles;
     return dispatch<true>(*st, bn, out_dtype, *ta, *tb, p, tiles,
                           static_cast<cudaStream_t>(stream));
+}
+
+// Contiguous grouped GEMM that allocates nothing: the CTA-pair kernel with its
+// stream-K scratch in g_noalloc_scratch instead of a cudaMalloc'd workspace.
+int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_layout,
+                                    int64_t ld_sa, const void* b, const float* scale_b,
+                                    const int32_t* grouped_layout, void* d, int out_dtype,
+                                    int64_t m_sum, int64_t n, int64_t k, int64_t num_groups,
+                                    void* stream) {
+    if (m_sum < 0 || m_sum > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (m_sum == 0) {
+        if (n <= 0 || k <= 0 || n % 128 || k % 128 || num_groups < 1 ||
+            (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16) ||
+            (sa_layout != FP8BS_SA_MK && sa_layout != FP8BS_SA_KM))
+            return FP8BS_ERR_INVALID_ARG;
+        return FP8BS_OK;
+    }
+    int v = validate_common(a, scale_a, sa_layout, ld_sa, b, scale_b, d, out_dtype, m_sum, n, k,
+                            num_groups);
+    if (v != FP8BS_OK) return v;
+    if (!grouped_layout || !aligned(grouped_layout, 4)) return FP8BS_ERR_INVALID_ARG;
+    // only shapes the CTA-pair kernel takes
+    const int64_t m_tiles = (m_sum + 127) / 128;
+    if (n % 256 != 0 || !aligned(d, 32) || m_tiles > fp8bs::kPairMaxTiles || num_groups >= (1 << 18))
+        return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    NoAllocDevice& nd = g_noalloc[dev];
+    if (!nd.ready) {
+        // once per device, with that device current: the device address of the array
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        nd.scratch = static_cast<unsigned char*>(addr);
+        nd.ready = true;
+    }
+    CUtensorMap ta, tb;
+    if ((rc = encode_map3_noalloc(a, k, m_sum, &ta)) != FP8BS_OK) return rc;
+    if ((rc = encode_map3_noalloc(b, k, num_groups * n, &tb)) != FP8BS_OK) return rc;
+
+    GemmParams p{};
+    p.sa = scale_a;
+    p.sb = scale_b;
+    p.row_info = grouped_layout;
+    p.d = d;
+    p.err = st->err;
+    p.rows = m_sum;
+    p.sa_g_stride = 0;
+    p.sa_kb_stride = sa_layout == FP8BS_SA_KM ? ld_sa : 1;
+    p.sa_row_stride = sa_layout == FP8BS_SA_KM ? 1 : k / 128;
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(k / 128);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>(m_tiles);
+    p.num_n_tiles = static_cast<int>(n / 256);
+    p.raster_band = 8;
+    const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return out_dtype == FP8BS_OUT_BF16
+               ? launch_pair_noalloc<__nv_bfloat16>(*st, nd, 0, ta, tb, p, tiles, s)
+               : launch_pair_noalloc<__half>(*st, nd, 1, ta, tb, p, tiles, s);
 }
 
 int fp8bs_device_error(int device, uint32_t* flags) {

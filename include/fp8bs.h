@@ -119,6 +119,40 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
                         int64_t expected_m, void* d, int out_dtype, int64_t num_groups,
                         int64_t m_max, int64_t n, int64_t k, void* stream);
 
+/*
+ * Contiguous grouped GEMM that allocates no device memory.  (No counterpart on
+ * the pages: an addition for callers that may not call cudaMalloc -- for
+ * example code that runs under a memory pool or allocator that owns all device
+ * memory, inside an allocation-free inference runtime, or while another
+ * component forbids allocations on the device.)
+ *
+ * Same arguments and results as gemm_grouped_contiguous.  It runs the CTA-pair
+ * kernel, whose stream-K scratch (fp32 partial tiles and their slot counters)
+ * lives in a statically sized device array of this library instead of a
+ * cudaMalloc'd workspace:
+ *  - size: 160 slots of 128 x 256 fp32 (2 per CTA pair, up to 80 pairs) plus
+ *    1280 bytes of counters, about 20 MiB; every GPU that loads the library
+ *    holds it until the process exits;
+ *  - the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before capturing the stream into a CUDA graph;
+ *  - every call clears the slot counters (cudaMemsetAsync on `stream`) and
+ *    then launches; calls share the array, so calls that overlap on the GPU
+ *    (for instance on two streams at once) race and give wrong results;
+ *  - no cudaMalloc, cudaFree or other allocating routine is called, and the
+ *    TMA tensor maps are encoded on the stack for every call.
+ * Returns FP8BS_ERR_INVALID_ARG, in addition to the cases of
+ * gemm_grouped_contiguous, for shapes the CTA-pair kernel does not take
+ * (n % 256 != 0, d not 32-byte aligned, m_sum > 524288 rows, num_groups >= 2^18)
+ * and when the device would run more than 80 CTA pairs (more scratch than the
+ * array holds).
+ */
+int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_layout,
+                                    int64_t ld_sa, const void* b, const float* scale_b,
+                                    const int32_t* grouped_layout, void* d, int out_dtype,
+                                    int64_t m_sum, int64_t n, int64_t k, int64_t num_groups,
+                                    void* stream);
+
 /* Synchronises `device`, returns the FP8BS_DEVERR_* bits recorded since the
  * last call in *flags and clears them.  Returns FP8BS_ERR_DEVICE when any bit
  * was set, FP8BS_OK otherwise (or FP8BS_ERR_CUDA / _INVALID_ARG). */

@@ -117,3 +117,28 @@ def test_scale_layout_from_strides():
     assert _binding._sa_layout_3d(m3, 3, 5, KB) == (fb.SA_MK, KB)
     s3 = torch.zeros(3, KB, 8)
     assert _binding._sa_layout_3d(s3[:, :, :5].transpose(1, 2), 3, 5, KB) == (fb.SA_KM, 8)
+
+
+def _noalloc(**kw):
+    args = dict(a=P, sa=P, sa_layout=0, ld_sa=0, b=P, sb=P, lay=P, d=P, out=0,
+                m_sum=256, n=256, k=256, g=2)
+    args.update(kw)
+    return _binding.gemm_grouped_contiguous_noalloc_raw(
+        args["a"], args["sa"], args["sa_layout"], args["ld_sa"], args["b"], args["sb"],
+        args["lay"], args["d"], args["out"], args["m_sum"], args["n"], args["k"], args["g"], 0)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n=384),                 # the CTA-pair kernel needs N % 256 == 0
+    dict(d=P + 16),              # and a 32-byte aligned D
+    dict(m_sum=524288 + 128),    # and at most 4096 row tiles
+    dict(g=1 << 18),             # and fewer than 2^18 groups
+    dict(a=0), dict(k=100), dict(out=5),
+])
+def test_noalloc_rejects(lib, bad):
+    assert _noalloc(**bad) == INVALID
+
+
+def test_noalloc_empty_is_noop(lib):
+    assert _noalloc(m_sum=0, a=0) == OK
+

@@ -64,7 +64,7 @@ struct GemmParams {
     int raster_band;             // contiguous: m-tiles per rasterisation band
     // stream-K tail of the CTA-pair kernel (sk_slots == 0 disables it)
     float* sk_partial;           // sk_slots x [128 rows x 256 cols] fp32 partial accumulators
-    uint32_t* sk_flags;          // 2 words per slot (ready warps, consumed warps), 0 between launches
+    uint32_t* sk_flags;          // 2 words per slot (ready tail warps; spare), 0 between launches
     int sk_slots;                // slots available (needs 2 per CTA pair of the grid)
 };
 

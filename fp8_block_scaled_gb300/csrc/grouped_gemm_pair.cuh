@@ -22,10 +22,14 @@
 // most once, into a head [0, x) finished last by one pair and a tail [x, end)
 // finished first by the next pair.  Each epilogue warp of the tail writes its
 // rows of the fp32 partial accumulator to a scratch slot and counts itself in
-// the slot's ready word; each epilogue warp of the head waits (bounded) until
-// all four have, adds the partial, and the last of them resets the slot's
-// words to zero for the next launch.  No warp waits on another warp of its
-// own CTA, so a warp that aborts cannot block the others.
+// the slot's ready word.  The head is always its pair's last piece, so once
+// its accumulator is complete the operand stages are idle: one thread of the
+// head waits (bounded) until all four tail warps have counted themselves,
+// copies the 128 KB slot into the stages with four bulk copies, and resets
+// the ready word for the next launch; every epilogue warp then adds the
+// partial chunk by chunk from shared memory.  Reading the partial with plain
+// loads instead left four dependent round trips to a remote L2 slice exposed
+// at the very end of the kernel.
 //
 // Operand staging: each pipeline stage holds two 128-K blocks, fetched with
 // one 3-D TMA box per operand (128 bytes x 128 rows x 2 blocks); the A and B
@@ -71,8 +75,10 @@ struct PairLayout {
     static constexpr int kOffSbRaw = kOffSaRaw + kStages * kKbPerStage * kSaRawBytes;
     static constexpr int kOffBar =
         (kOffSbRaw + kStages * kKbPerStage * kSbRawBytes + 7) / 8 * 8;
-    // full[S], empty[S], sf_raw[S], tmem_full, tmem_empty, drain
-    static constexpr int kNumBars = 3 * kStages + 3;
+    // full[S], empty[S], sf_raw[S], tmem_full, tmem_empty, drain, partial[4]
+    static constexpr int kPartChunks = 4;                   // stream-K partial, 64 columns each
+    static constexpr int kPartChunkBytes = 128 * 64 * 4;
+    static constexpr int kNumBars = 3 * kStages + 3 + kPartChunks;
     static constexpr int kPrefetchStages = 3;  // stages of A/B prefetched into L2 ahead of the ring
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // slot, abort, scan scratch
     static constexpr int kMiscBytes = 16 + 2 * 8 * 4;
@@ -85,6 +91,8 @@ struct PairLayout {
     static_assert(256 + kStages * kKbPerStage * kSfColsPerKb <= kTmemCols, "TMEM budget");
     static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
     static_assert(kPairMaxTiles * 4 <= kStages * kAStageBytes, "prologue scratch");
+    static_assert(kPartChunks * kPartChunkBytes <= kStages * (kAStageBytes + kBStageBytes),
+                  "stream-K partial staging");
 };
 
 // Contiguous pair-list entry: first 128-row tile (12 bits), "second tile not
@@ -196,6 +204,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const uint32_t bar_tmem_full = sbase + L::kOffBar + 8u * (3 * S);
     const uint32_t bar_tmem_empty = sbase + L::kOffBar + 8u * (3 * S + 1);
     const uint32_t bar_drain = sbase + L::kOffBar + 8u * (3 * S + 2);
+    auto bar_part = [&](int c) { return sbase + L::kOffBar + 8u * (3 * S + 3 + c); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
     int* scan_scratch = reinterpret_cast<int*>(smem + L::kOffMisc + 16);
@@ -214,6 +223,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         mbar_init(bar_tmem_full, 1);
         mbar_init(bar_tmem_empty, 8);        // 4 epilogue warps x 2 CTAs
         mbar_init(bar_drain, 1);
+        for (int c = 0; c < L::kPartChunks; ++c) mbar_init(bar_part(c), 1);  // one use per launch
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -670,10 +680,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 if (lane == 0) atomicAdd(p.sk_flags + 2 * slot, 1u);
             } else {
-                // head: wait until the four tail warps of the same unit (the next pair's
-                // first piece) have published their rows, add the partial, store
+                // head (the pair's last piece; every MMA reading the stages has completed)
                 const int slot = (pair_id + 1) * 2 + static_cast<int>(rank);
-                if (lane == 0) {
+                if (warp == 4 && lane == 0) {
                     const uint64_t t0 = global_timer_ns();
                     while (ld_acquire_gpu_u32(p.sk_flags + 2 * slot) < 4u) {
                         if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
@@ -681,12 +690,20 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                             break;
                         }
                     }
+                    // the copies are issued even after a time-out, so that no warp
+                    // waits for them in vain (the error is already recorded)
+                    fence_proxy_async_global();
+                    const float* src = p.sk_partial + static_cast<int64_t>(slot) * (128 * 256);
+#pragma unroll
+                    for (int c = 0; c < L::kPartChunks; ++c) {
+                        mbar_arrive_expect_tx(bar_part(c), L::kPartChunkBytes);
+                        bulk_load(sbase + L::kOffA + c * L::kPartChunkBytes,
+                                  src + c * (L::kPartChunkBytes / 4), L::kPartChunkBytes,
+                                  bar_part(c));
+                    }
                 }
-                __syncwarp();
-                const float* part =
-                    p.sk_partial + static_cast<int64_t>(slot) * (128 * 256) + row_in_half * 8;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < L::kPartChunks; ++c) {
                     uint32_t v[64];
                     tc_ld_32x32b_x64_sync(trow + c * 64, v);
                     if (c == 3) {
@@ -694,13 +711,19 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         __syncwarp();
                         if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
                     }
+                    if (!pair_warp_wait(bar_part(c), 0, abort_flag, peer_abort, p.err)) {
+                        aborted = true;
+                        break;
+                    }
+                    // chunk c: [8 column groups][128 rows][8 columns] fp32
+                    const float* part = reinterpret_cast<const float*>(
+                                            smem + L::kOffA + c * L::kPartChunkBytes) +
+                                        row_in_half * 8;
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        // L2-only loads: this SM may hold stale L1 lines of the slot from an
-                        // earlier launch
-                        const float4 f = __ldcg(reinterpret_cast<const float4*>(
-                            part + (c * 8 + i / 2) * (128 * 8) + 4 * (i & 1)));
+                        const float4 f = *reinterpret_cast<const float4*>(
+                            part + (i >> 1) * (128 * 8) + 4 * (i & 1));
                         pk[2 * i] = pack2<OutT>(__uint_as_float(v[4 * i]) + f.x,
                                                 __uint_as_float(v[4 * i + 1]) + f.y);
                         pk[2 * i + 1] = pack2<OutT>(__uint_as_float(v[4 * i + 2]) + f.z,
@@ -715,15 +738,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         }
                     }
                 }
-                // the last of the four head warps to finish reading resets the slot
-                __syncwarp();
-                if (lane == 0) {
-                    __threadfence();
-                    if (atomicAdd(p.sk_flags + 2 * slot + 1, 1u) == 3u) {
-                        p.sk_flags[2 * slot] = 0u;
-                        p.sk_flags[2 * slot + 1] = 0u;
-                    }
-                }
+                // the slot has been copied out (all four copies completed): ready for
+                // the next launch
+                if (warp == 4 && lane == 0 && !aborted) p.sk_flags[2 * slot] = 0u;
+                if (aborted) break;
             }
             acc_ph ^= 1u;
         }

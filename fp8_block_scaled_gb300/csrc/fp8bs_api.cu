@@ -198,6 +198,16 @@ int get_map3(int dev, const void* ptr, uint64_t inner, uint64_t outer, uint32_t 
     return FP8BS_OK;
 }
 
+// Programmatic dependent launch: every kernel executes griddepcontrol.wait
+// before it touches device memory, so it may be scheduled while the grid it
+// follows in the stream is still finishing (its CTAs start on the SMs that
+// grid has already freed); after a grid that never signals, or after a
+// non-kernel stream operation, the launch is ordered as usual.
+inline void set_pdl(cudaLaunchAttribute& a) {
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+}
+
 template <int BN, typename OutT, bool kMasked>
 int launch(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensorMap& tb,
            const GemmParams& p, int64_t tiles_bound, cudaStream_t stream) {
@@ -214,8 +224,20 @@ int launch(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensor
     }
     const int grid = static_cast<int>(tiles_bound < st.sms ? tiles_bound : st.sms);
     if (grid <= 0) return FP8BS_OK;
-    kern<<<grid, fp8bs::kThreads, smem, stream>>>(ta, tb, p);
-    return cudaGetLastError() == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    set_pdl(attr[0]);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(fp8bs::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_OK;
 }
 
 // CTA-pair kernel: cluster of 2, persistent over at most the number of pairs
@@ -227,16 +249,17 @@ int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUt
     auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, kMasked>;
     const int smem = L::kBytes + L::kAlignSlack;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl(attr[1]);
     cfg.blockDim = dim3(fp8bs::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
     if (!st.attr_set[attr_slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess) {
@@ -265,6 +288,7 @@ int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUt
         q.sk_slots = w->slots;
     }
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, q) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
@@ -365,16 +389,17 @@ int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUte
     auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, false>;
     const int smem = L::kBytes + L::kAlignSlack;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    set_pdl(attr[1]);
     cfg.blockDim = dim3(fp8bs::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
     if (!nd.attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess) {
@@ -404,6 +429,7 @@ int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUte
     q.sk_flags = flags;
     q.sk_slots = kNoAllocSlots;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, q) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;

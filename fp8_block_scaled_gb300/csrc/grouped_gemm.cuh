@@ -241,6 +241,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
     }
+    // inputs, outputs and the error word may belong to the grid this launch
+    // follows (programmatic dependent launch): wait for it before touching them
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (warp == 2) {
         tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
         tmem_relinquish();

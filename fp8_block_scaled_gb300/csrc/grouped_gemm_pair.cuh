@@ -91,6 +91,7 @@ struct PairLayout {
     static_assert(256 + kStages * kKbPerStage * kSfColsPerKb <= kTmemCols, "TMEM budget");
     static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
     static_assert(kPairMaxTiles * 4 <= kStages * kAStageBytes, "prologue scratch");
+    static_assert(kPairMaxTiles % kThreads == 0, "grouped_layout loads per thread");
     static_assert(kPartChunks * kPartChunkBytes <= kStages * (kAStageBytes + kBStageBytes),
                   "stream-K partial staging");
 };
@@ -231,6 +232,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
     }
+    // Everything above touches only this CTA and the kernel parameters; from
+    // here on the inputs (and the outputs and scratch) may belong to the grid
+    // this launch follows, so wait for it, then let a grid launched after this
+    // one with programmatic serialization be scheduled onto the SMs this grid
+    // frees (it waits for this grid's completion in its own wait).
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (warp == 2) {
         tmem_alloc_pair(smem_addr(tmem_slot), L::kTmemCols);
         tmem_relinquish_pair();
@@ -241,13 +249,25 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         // ---- pair list: tiles of each expert segment, two by two
         const int T = p.num_m_tiles;
         int* E = reinterpret_cast<int*>(smem + L::kOffA);  // scratch (stage buffers are idle)
-        for (int t = threadIdx.x; t < T; t += kThreads) {
-            int v = __ldg(p.row_info + static_cast<int64_t>(t) * kBM);
-            if (v >= p.num_groups || v < -1) {
-                raise_error(p.err, kErrBadGroup);
-                v = -1;
+        // all of this thread's grouped_layout reads are issued before the first is used
+        constexpr int kLoads = kPairMaxTiles / kThreads;
+        int ev[kLoads];
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j) {
+            const int t = static_cast<int>(threadIdx.x) + j * kThreads;
+            ev[j] = t < T ? __ldg(p.row_info + static_cast<int64_t>(t) * kBM) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j) {
+            const int t = static_cast<int>(threadIdx.x) + j * kThreads;
+            if (t < T) {
+                int v = ev[j];
+                if (v >= p.num_groups || v < -1) {
+                    raise_error(p.err, kErrBadGroup);
+                    v = -1;
+                }
+                E[t] = v;
             }
-            E[t] = v;
         }
         __syncthreads();
         const int chunk = (T + kThreads - 1) / kThreads;

@@ -27,7 +27,13 @@
  *    for the transposed activation-scale layout, whose ld_sa must be a
  *    multiple of 4).  N and K must be positive multiples of 128.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
- *    asynchronous: they validate, enqueue one kernel and return.
+ *    asynchronous: they validate, enqueue one kernel and return.  The kernel
+ *    is launched with programmatic stream serialization: its CTAs may be
+ *    scheduled while the preceding kernel on the stream is still finishing,
+ *    but each executes griddepcontrol.wait before it reads or writes device
+ *    memory, so stream order is kept.  Each kernel also signals
+ *    griddepcontrol.launch_dependents early, which lets a following kernel
+ *    launched the same way start on the SMs this one has freed.
  *  - Scratch: the CTA-pair kernel balances its last rounds with a stream-K
  *    split whose fp32 partial tiles live in a per-(device, stream) workspace
  *    (about 20 MB on a 152-SM GB300) that the library allocates with

@@ -249,23 +249,23 @@ def bench_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # A step is exactly one launch of the kernel, so the kernel's average launch
+    # duration is the timed region's event time over the step count.  Events
+    # recorded between the launches would stand between two kernels of the
+    # stream and keep the next grid from being scheduled while the previous one
+    # finishes (programmatic dependent launch), so there are none.
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
     t0.record(stream)
     for i in range(args.steps):
-        starts[i].record(stream)
         run_once(fb, p, *bufs[i % sets])
-        ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    per_launch = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     if fb.device_error(local):
         raise RuntimeError("device error word set during the timed region")
     ms_per_step = max_over_ranks(elapsed_ms / args.steps, world, dev)
@@ -275,7 +275,7 @@ def bench_ours(args):
 
     # roofline of the one kernel on the path
     peaks, peaks_kind = load_peaks()
-    mean_launch_ms = statistics.fmean(per_launch)
+    mean_launch_ms = elapsed_ms / args.steps
     achieved = flops / (mean_launch_ms * 1e-3) / 1e12
     peak_fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
     alg_bytes = p.algorithmic_bytes(out_bytes=2)

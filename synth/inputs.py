@@ -1,10 +1,12 @@
 """Seeded workload generator and UE8M0 block quantiser (input recipe only).
 
-Shapes of the five workloads follow the coverage named on the FlyDSL PR #433
+Shapes of the named workloads follow the coverage named on the FlyDSL PR #433
 page ("Adds Grouped and Batched GEMM kernels with blockscaling matching
 DeepGEMM API", *Test plan*): 1-8 (and 16/32) groups, m_per_group from the
 unaligned 100 up to 1024, the DeepSeek-V3 expert shapes N=2048/K=7168 and
-N=7168/K=2304, bf16 and f16 outputs.
+N=7168/K=2304, bf16 and f16 outputs; plus the dense 4096 x 4096 x 16384 shape of the
+FP8 figure on the "[Kernel][MI350] Add cache-aware 8-wave BF16/FP16 GEMM" page
+(*Performance*), run as a single group.
 
 All draws are seeded.  Group sizes come from numpy's PCG64 (identical on every
 platform); the N(0,1) data comes from a torch generator on the chosen device,
@@ -48,6 +50,12 @@ CONFIGS: Dict[str, dict] = {
     "c5_contig_g32_dirichlet_n4096_k7168": dict(
         variant="contiguous", G=32, N=4096, K=7168, out=OUT_BF16, sa_layout=SA_MK,
         sizes=("dirichlet", 0.5, 65536), seed=5),
+    # dense GEMM as the G = 1 case of the contiguous layout: 4096 x 4096 x 16384, the
+    # FP8 shape whose throughput the pages publish (there with row scales, on other
+    # hardware; here block-scaled like every other workload)
+    "c6_dense_g1_m4096_n4096_k16384": dict(
+        variant="contiguous", G=1, N=4096, K=16384, out=OUT_BF16, sa_layout=SA_MK,
+        sizes=("fixed", 4096), seed=6),
 }
 
 
@@ -288,7 +296,7 @@ def make_problem(variant: str, G: int, N: int, K: int, group_sizes, *, out_dtype
 
 
 def make_config(name: str, device="cpu") -> Problem:
-    """One of the five named workloads."""
+    """One of the named workloads of CONFIGS."""
     c = CONFIGS[name]
     sizes = draw_group_sizes(c["sizes"], c["G"], c["seed"])
     return make_problem(c["variant"], c["G"], c["N"], c["K"], sizes, out_dtype=c["out"],

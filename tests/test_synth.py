@@ -1,6 +1,6 @@
 """The seeded input recipe (CPU only): the generator's quantiser against the
 oracle's independently written E4M3 encoder and ceil_to_ue8m0, and the group
-size draws of the five workloads."""
+size draws of the named workloads."""
 import numpy as np
 import torch
 

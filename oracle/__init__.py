@@ -27,6 +27,14 @@ Parity status of every function (see tests/test_oracle_pins.py):
                     pre-quantisation fp32 product within calc_diff 1e-3
   calc_diff         pinned: closed forms
   block_dot_exact   pinned: exact-rational brute force
+  silu_mul_quant    pinned: hand-derived golden blocks, SiLU closed forms and the
+                    identity silu(x) - silu(-x) = x, quantiser invariants (power-of-two
+                    scale, |h|/s <= 448, half-spacing error, sign), zero blocks
+
+The fused gate/up epilogue (silu_mul_quant) follows "flydsl mxfp4 a4w4 MoE:
+bring gemm1/gemm2 to parity with the HIP backend" (aiter PR #3828), section
+*gemm1* (silu_mul of the gate and up halves), and requantises with the (1,128)
+UE8M0 ceil quantiser of the FlyDSL PR #433 page, *DeepGEMM conformance details*.
 """
 from __future__ import annotations
 
@@ -76,6 +84,8 @@ def _load():
     lib.fp8bs_oracle_calc_diff.restype = ctypes.c_double
     lib.fp8bs_oracle_block_dot_exact.argtypes = [_P, _P]
     lib.fp8bs_oracle_block_dot_exact.restype = ctypes.c_double
+    lib.fp8bs_oracle_silu_mul_quant.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P]
+    lib.fp8bs_oracle_silu_mul_quant.restype = ctypes.c_int
     lib.fp8bs_oracle_max_threads.argtypes = []
     lib.fp8bs_oracle_max_threads.restype = ctypes.c_int
     _lib = lib
@@ -223,3 +233,37 @@ def grouped_masked(a_codes, scale_a, sa_layout, b_codes, scale_b, masked_m,
     if rc != 0:
         raise ValueError("oracle: invalid arguments")
     return acc, valid.astype(bool), rows
+
+
+# ----------------------------------------------------------------- fused gate/up epilogue
+def silu_mul_quant(acc_gate_up):
+    """SiLU(gate) * up of a [rows, 2I] accumulator (gate = columns [0, I), up =
+    [I, 2I)), requantised per (1,128) block to E4M3 with UE8M0 ceil scales.
+
+    Returns a dict of numpy arrays:
+      h        fp64  [rows, I]      the exact activation
+      q        uint8 [rows, I]      E4M3 codes
+      s        fp32  [rows, I/128]  power-of-two scales
+      margin   fp64  [rows, I]      relative distance of fl32(h)/s to the nearest
+                                    E4M3 rounding boundary
+      tmargin  fp64  [rows, I/128]  relative distance of amax/448 to the nearest
+                                    power of two
+    """
+    acc = _c(acc_gate_up, np.float64)
+    rows, n2 = acc.shape
+    if n2 % 256:
+        raise ValueError("silu_mul_quant: the accumulator needs 2I columns, I % 128 == 0")
+    i_out = n2 // 2
+    h = np.empty((rows, i_out), dtype=np.float64)
+    q = np.empty((rows, i_out), dtype=np.uint8)
+    s = np.empty((rows, i_out // 128), dtype=np.float32)
+    margin = np.empty((rows, i_out), dtype=np.float64)
+    tmargin = np.empty((rows, i_out // 128), dtype=np.float64)
+    gate = np.ascontiguousarray(acc[:, :i_out])
+    up = np.ascontiguousarray(acc[:, i_out:])
+    rc = _load().fp8bs_oracle_silu_mul_quant(_ptr(gate), _ptr(up), rows, i_out, i_out,
+                                             _ptr(h), _ptr(q), _ptr(s), _ptr(margin),
+                                             _ptr(tmargin))
+    if rc != 0:
+        raise ValueError("oracle: invalid arguments")
+    return {"h": h, "q": q, "s": s, "margin": margin, "tmargin": tmargin}

@@ -308,3 +308,85 @@ double fp8bs_oracle_block_dot_exact(const uint8_t* x, const uint8_t* y) {
     }
     return ldexp((double)total, -18);
 }
+
+/* ------------------------------------------------------------------------
+ * Fused MoE gate/up epilogue: SiLU(gate) * up, requantised for the down
+ * projection.
+ *
+ * [P3] "flydsl mxfp4 a4w4 MoE: bring gemm1/gemm2 to parity with the HIP
+ *      backend", section gemm1: the first MoE GEMM ends in silu_mul, i.e. the
+ *      SiLU of the gate half of its output times the up half.
+ * [P1] Summary and DeepGEMM conformance details: the down projection consumes
+ *      E4M3 activations with (1,128) UE8M0 ceil scales, the quantiser of the
+ *      inputs (amax / 448, ceil to a power of two, round to nearest even).
+ *
+ * gate, up: the fp64 accumulators of the two halves, rows x I, row stride ld.
+ * For every row and column j < I:
+ *     h = gate / (1 + exp(-gate)) * up                            (fp64)
+ * and per 128-column block of a row:
+ *     amax = max |h| (at least 1e-4, the reading for an all-zero block),
+ *     t = fl32(fl32(amax) / 448), s = ceil_to_ue8m0(t),
+ *     q = e4m3_rne(fl32(h) / s)
+ * The scale exponent and the codes are decided in fp32 (the kernel's
+ * precision; the pages fix none).  Outputs, all rows x I unless noted:
+ *     h       the exact (fp64) activation;
+ *     q       E4M3 codes;
+ *     s       [rows, I/128] scales;
+ *     margin  relative distance of fl32(h)/s to the nearest E4M3 rounding
+ *             boundary (the midpoint between two neighbouring values);
+ *     tmargin [rows, I/128] relative distance of amax/448 (fp64) to the
+ *             nearest power of two.
+ * Where a margin is tiny, an accumulator that differs from the exact one in
+ * its last fp32 bits may round to the other neighbour (several results are
+ * correct); everywhere else the code and the scale are unique.
+ * ------------------------------------------------------------------------ */
+static double e4m3_boundary_margin(double x) {
+    /* boundaries between neighbouring non-negative E4M3 values, and the
+     * relative distance of |x| to the nearest of them */
+    double ax = fabs(x), best = INFINITY, prev, cur, mid, d;
+    int c;
+    prev = fp8bs_oracle_e4m3_to_double(0);
+    for (c = 1; c <= 0x7E; ++c) {
+        cur = fp8bs_oracle_e4m3_to_double((uint8_t)c);
+        mid = 0.5 * (prev + cur);
+        d = fabs(ax - mid);
+        if (d < best) best = d;
+        prev = cur;
+    }
+    return best / (ax > ldexp(1.0, -9) ? ax : ldexp(1.0, -9));
+}
+
+int fp8bs_oracle_silu_mul_quant(const double* gate, const double* up, int64_t rows, int64_t ld,
+                                int64_t I, double* h, uint8_t* q, float* s, double* margin,
+                                double* tmargin) {
+    int64_t r;
+    if (rows < 0 || I <= 0 || I % 128 != 0 || ld < I) return 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (r = 0; r < rows; ++r) {
+        int64_t jb, j;
+        for (jb = 0; jb < I / 128; ++jb) {
+            double amax = 0.0, t64, f;
+            float t, sc;
+            int E;
+            for (j = jb * 128; j < jb * 128 + 128; ++j) {
+                const double g = gate[r * ld + j];
+                const double v = g / (1.0 + exp(-g)) * up[r * ld + j];
+                h[r * I + j] = v;
+                if (fabs(v) > amax) amax = fabs(v);
+            }
+            if (amax < 1e-4) amax = 1e-4;
+            t = (float)amax / 448.0f;
+            sc = (float)fp8bs_oracle_ceil_to_ue8m0((double)t);
+            s[r * (I / 128) + jb] = sc;
+            t64 = amax / 448.0;
+            f = frexp(t64, &E); /* t64 = f * 2^E, f in [0.5, 1) */
+            tmargin[r * (I / 128) + jb] = fmin(2.0 * f - 1.0, (1.0 - f) / f);
+            for (j = jb * 128; j < jb * 128 + 128; ++j) {
+                const float x = (float)h[r * I + j] / sc; /* exact: sc is a power of two */
+                q[r * I + j] = fp8bs_oracle_double_to_e4m3((double)x);
+                margin[r * I + j] = e4m3_boundary_margin((double)x);
+            }
+        }
+    }
+    return 0;
+}

@@ -189,10 +189,42 @@ def out_dtype_of(p):
 
 
 def run_once(fb, p, a, sa, b, sb, rowinfo, d, stream=None):
-    if p.variant == "contiguous":
+    if p.epilogue == "silu_mul_quant":
+        q, qs = d
+        if p.variant == "contiguous":
+            fb.gemm_grouped_contiguous_silu_mul_quant(a, sa, b, sb, q, qs, rowinfo, stream=stream)
+        else:
+            fb.gemm_grouped_masked_silu_mul_quant(a, sa, b, sb, q, qs, rowinfo, stream=stream)
+    elif p.variant == "contiguous":
         fb.gemm_grouped_contiguous(a, sa, b, sb, d, rowinfo, stream=stream)
     else:
         fb.gemm_grouped_masked(a, sa, b, sb, d, rowinfo, stream=stream)
+
+
+def alloc_out(p, dev, pinned=False):
+    """The step's output: D (bf16/f16), or for the fused epilogue the E4M3 codes and
+    their fp32 scales in the activation-scale layout of the workload.  Returns the
+    argument run_once takes and the list of underlying tensors (on the device, or
+    in pinned host memory)."""
+    lead = (p.rows,) if p.variant == "contiguous" else (p.G, p.M_max)
+    kw = {"pin_memory": True} if pinned else {"device": dev}
+    if p.epilogue != "silu_mul_quant":
+        d = torch.empty(lead + (p.N,), dtype=out_dtype_of(p), **kw)
+        return d, [d]
+    q = torch.empty(lead + (p.N // 2,), dtype=torch.uint8, **kw)
+    nblk = p.N // 256
+    if p.sa_layout == 0:
+        store = torch.empty(lead + (nblk,), dtype=torch.float32, **kw)
+        view = store
+    else:
+        ld = (lead[-1] + 3) // 4 * 4
+        if p.variant == "contiguous":
+            store = torch.empty((nblk, ld), dtype=torch.float32, **kw)
+            view = store[:, : lead[-1]].t()
+        else:
+            store = torch.empty((p.G, nblk, ld), dtype=torch.float32, **kw)
+            view = store[:, :, : lead[-1]].transpose(1, 2)
+    return (q, view), [q, store]
 
 
 def describe(p, l2_note):
@@ -204,6 +236,11 @@ def describe(p, l2_note):
            "parallelism": "replicas (no exchange step)", "l2": l2_note}
     if p.variant == "masked":
         cfg["M_max"] = p.M_max
+    if p.epilogue == "silu_mul_quant":
+        cfg["epilogue"] = ("SiLU(gate) * up of the B halves [0, N/2) and [N/2, N), requantised "
+                           "to E4M3 with (1,128) UE8M0 scales")
+        cfg["out"] = "e4m3 [rows, N/2] + fp32 scales " + (
+            "transposed [N/256, M]" if p.sa_layout == 1 else "[M, N/256]")
     return cfg
 
 
@@ -222,7 +259,6 @@ def bench_ours(args):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     sets = max(2, math.ceil(3 * l2 / in_bytes))
     bufs = []
-    d_shape = (p.rows, p.N) if p.variant == "contiguous" else (p.G, p.M_max, p.N)
     for i in range(sets):
         if i == 0:
             a, sa, b, sb, ri = p.a, sa_view, p.b, p.sb, rowinfo
@@ -234,7 +270,7 @@ def bench_ours(args):
                       else sa_store[:, :, : p.M_max].transpose(1, 2))
             else:
                 sa = sa_store
-        d = torch.empty(d_shape, dtype=out_dtype_of(p), device=dev)
+        d, _ = alloc_out(p, dev)
         bufs.append((a, sa, b, sb, ri, d))
     l2_note = (f"rotating {sets} input sets of {in_bytes / 1e6:.1f} MB "
                f"({sets * in_bytes / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)")
@@ -334,9 +370,8 @@ def bench_e2e(fb, p, dev, steps):
     rowinfo = p.grouped_layout if p.variant == "contiguous" else p.masked_m
     host = [t.cpu().pin_memory() for t in (p.a, p.sa, p.b, p.sb, rowinfo)]
     devb = [torch.empty_like(t, device=dev) for t in host]
-    d_shape = (p.rows, p.N) if p.variant == "contiguous" else (p.G, p.M_max, p.N)
-    d = torch.empty(d_shape, dtype=out_dtype_of(p), device=dev)
-    d_host = torch.empty(d_shape, dtype=out_dtype_of(p)).pin_memory()
+    d, d_dev = alloc_out(p, dev)
+    _, d_host = alloc_out(p, dev, pinned=True)
 
     def sa_view(sa):
         if p.sa_layout == 0:
@@ -347,7 +382,8 @@ def bench_e2e(fb, p, dev, steps):
         for h, g in zip(host, devb):
             g.copy_(h, non_blocking=True)
         run_once(fb, p, devb[0], sa_view(devb[1]), devb[2], devb[3], devb[4], d)
-        d_host.copy_(d, non_blocking=True)
+        for h, g in zip(d_host, d_dev):
+            h.copy_(g, non_blocking=True)
 
     for _ in range(2):
         step()
@@ -361,7 +397,7 @@ def bench_e2e(fb, p, dev, steps):
     torch.cuda.synchronize(dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
     return {"ms_per_step": t0.elapsed_time(t1) / steps, "h2d": h2d,
-            "d2h": d_host.numel() * d_host.element_size()}
+            "d2h": sum(t.numel() * t.element_size() for t in d_host)}
 
 
 def _oracle_call(p, host, rows):
@@ -369,8 +405,12 @@ def _oracle_call(p, host, rows):
 
     a, sa, b, sb, ri = host
     if p.variant == "contiguous":
-        return oracle.grouped_contiguous(a, sa, p.sa_layout, b, sb, ri, rows=rows, ld_sa=p.ld_sa)
-    return oracle.grouped_masked(a, sa, p.sa_layout, b, sb, ri, rows=rows, ld_sa=p.ld_sa)
+        res = oracle.grouped_contiguous(a, sa, p.sa_layout, b, sb, ri, rows=rows, ld_sa=p.ld_sa)
+    else:
+        res = oracle.grouped_masked(a, sa, p.sa_layout, b, sb, ri, rows=rows, ld_sa=p.ld_sa)
+    if p.epilogue == "silu_mul_quant":
+        oracle.silu_mul_quant(res[0])
+    return res
 
 
 def _host_inputs(p):

@@ -9,7 +9,9 @@ blockscaling matching DeepGEMM API" (FlyDSL PR #433), section Summary:
 E4M3 operands, (1,128) activation and (128,128) weight UE8M0 scales, fp32
 accumulation, bf16/f16 output, in a contiguous (grouped_layout, -1 = padding)
 and a masked (masked_m) variant.  All compute runs in the hand-written CUDA
-kernels of ``libfp8bs.so``; this package only marshals arguments.
+kernels of ``libfp8bs.so``; this package only marshals arguments.  The
+``*_silu_mul_quant`` entry points fuse the first MoE GEMM's SiLU(gate) * up and
+the (1,128) E4M3 requantisation of its output into the same kernel.
 """
 from ._binding import (  # noqa: F401
     DEVERR_BAD_GROUP,
@@ -28,8 +30,12 @@ from ._binding import (  # noqa: F401
     gemm_grouped_contiguous,
     gemm_grouped_contiguous_noalloc_raw,
     gemm_grouped_contiguous_raw,
+    gemm_grouped_contiguous_silu_mul_quant,
+    gemm_grouped_contiguous_silu_mul_quant_raw,
     gemm_grouped_masked,
     gemm_grouped_masked_raw,
+    gemm_grouped_masked_silu_mul_quant,
+    gemm_grouped_masked_silu_mul_quant_raw,
     lib_path,
     load,
     status_string,

@@ -29,6 +29,7 @@ DEVERR_BAD_GROUP = 0x8
 
 # every symbol include/fp8bs.h declares
 EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "gemm_grouped_contiguous_noalloc",
+           "gemm_grouped_contiguous_silu_mul_quant", "gemm_grouped_masked_silu_mul_quant",
            "fp8bs_device_error", "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version")
 
 _lib = None
@@ -68,6 +69,12 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.gemm_grouped_contiguous_noalloc.argtypes = [_P, _P, _I, _I64, _P, _P, _P, _P, _I,
                                                         _I64, _I64, _I64, _I64, _P]
         lib.gemm_grouped_contiguous_noalloc.restype = _I
+        lib.gemm_grouped_contiguous_silu_mul_quant.argtypes = [_P, _P, _I, _I64, _P, _P, _P, _P, _P,
+                                                               _I, _I64, _I64, _I64, _I64, _I64, _P]
+        lib.gemm_grouped_contiguous_silu_mul_quant.restype = _I
+        lib.gemm_grouped_masked_silu_mul_quant.argtypes = [_P, _P, _I, _I64, _P, _P, _P, _I64, _P,
+                                                           _P, _I, _I64, _I64, _I64, _I64, _I64, _P]
+        lib.gemm_grouped_masked_silu_mul_quant.restype = _I
         lib.fp8bs_device_error.argtypes = [_I, ctypes.POINTER(ctypes.c_uint32)]
         lib.fp8bs_device_error.restype = _I
         lib.fp8bs_status_string.argtypes = [_I]
@@ -222,6 +229,91 @@ def gemm_grouped_masked(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0
                                  _out_code(d), G, m_max, n, k, stream)
     _check(st, "gemm_grouped_masked")
     return d
+
+
+def gemm_grouped_contiguous_silu_mul_quant_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr,
+                                               layout_ptr, out_ptr, out_scale_ptr,
+                                               out_scale_layout, ld_out_scale, m_sum, n, k,
+                                               num_groups, stream=None) -> int:
+    lib = load()
+    return lib.gemm_grouped_contiguous_silu_mul_quant(
+        a_ptr, sa_ptr, int(sa_layout), int(ld_sa), b_ptr, sb_ptr, layout_ptr, out_ptr,
+        out_scale_ptr, int(out_scale_layout), int(ld_out_scale), int(m_sum), int(n), int(k),
+        int(num_groups), ctypes.c_void_p(_stream_handle(stream)))
+
+
+def gemm_grouped_masked_silu_mul_quant_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr,
+                                           masked_m_ptr, expected_m, out_ptr, out_scale_ptr,
+                                           out_scale_layout, ld_out_scale, num_groups, m_max, n,
+                                           k, stream=None) -> int:
+    lib = load()
+    return lib.gemm_grouped_masked_silu_mul_quant(
+        a_ptr, sa_ptr, int(sa_layout), int(ld_sa), b_ptr, sb_ptr, masked_m_ptr, int(expected_m),
+        out_ptr, out_scale_ptr, int(out_scale_layout), int(ld_out_scale), int(num_groups),
+        int(m_max), int(n), int(k), ctypes.c_void_p(_stream_handle(stream)))
+
+
+def _check_out(out, out_scale, lead, n):
+    if out.dtype not in (torch.float8_e4m3fn, torch.uint8) or not out.is_contiguous():
+        raise TypeError("out must be a contiguous float8_e4m3fn (or uint8) tensor")
+    if out.shape != tuple(lead) + (n // 2,):
+        raise ValueError(f"out must be {tuple(lead) + (n // 2,)}")
+    if out_scale.dtype != torch.float32:
+        raise TypeError("out_scale must be fp32")
+
+
+def gemm_grouped_contiguous_silu_mul_quant(a, scale_a, b, scale_b, out, out_scale,
+                                           grouped_layout, *, stream=None):
+    """Fused gate/up GEMM + SiLU(gate) * up + (1,128) E4M3 requantisation (include/fp8bs.h).
+
+    b [G, N, K] holds the gate rows [0, N/2) and the up rows [N/2, N) of each
+    expert.  out [M_sum, N/2] receives E4M3 codes; out_scale is the logical
+    [M_sum, N/256] fp32 scale tensor (row-major, or a transposed view of a
+    [N/256, ld] buffer) -- the activation operand of the down projection.
+    Rows marked -1 are not written.
+    """
+    m_sum, k = a.shape
+    G, n, kb_ = b.shape
+    if kb_ != k or grouped_layout.shape != (m_sum,) or grouped_layout.dtype != torch.int32:
+        raise ValueError("shape mismatch")
+    if scale_b.shape != (G, n // 128, k // 128) or scale_b.dtype != torch.float32:
+        raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
+    _check_out(out, out_scale, (m_sum,), n)
+    for t in (a, scale_a, b, scale_b, out, out_scale, grouped_layout):
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+    layout, ld = _sa_layout_2d(scale_a, m_sum, k // 128)
+    olayout, old = _sa_layout_2d(out_scale, m_sum, n // 256)
+    st = gemm_grouped_contiguous_silu_mul_quant_raw(
+        _fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
+        scale_b.contiguous().data_ptr(), grouped_layout.contiguous().data_ptr(), out.data_ptr(),
+        out_scale.data_ptr(), olayout, old, m_sum, n, k, G, stream)
+    _check(st, "gemm_grouped_contiguous_silu_mul_quant")
+    return out, out_scale
+
+
+def gemm_grouped_masked_silu_mul_quant(a, scale_a, b, scale_b, out, out_scale, masked_m,
+                                       expected_m: int = 0, *, stream=None):
+    """Masked variant: a [G, M_max, K]; out [G, M_max, N/2]; out_scale logical
+    [G, M_max, N/256] (row-major or a transposed view of [G, N/256, ld])."""
+    G, m_max, k = a.shape
+    Gb, n, kb_ = b.shape
+    if Gb != G or kb_ != k or masked_m.shape != (G,) or masked_m.dtype != torch.int32:
+        raise ValueError("shape mismatch")
+    if scale_b.shape != (G, n // 128, k // 128) or scale_b.dtype != torch.float32:
+        raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
+    _check_out(out, out_scale, (G, m_max), n)
+    for t in (a, scale_a, b, scale_b, out, out_scale, masked_m):
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+    layout, ld = _sa_layout_3d(scale_a, G, m_max, k // 128)
+    olayout, old = _sa_layout_3d(out_scale, G, m_max, n // 256)
+    st = gemm_grouped_masked_silu_mul_quant_raw(
+        _fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
+        scale_b.contiguous().data_ptr(), masked_m.contiguous().data_ptr(), expected_m,
+        out.data_ptr(), out_scale.data_ptr(), olayout, old, G, m_max, n, k, stream)
+    _check(st, "gemm_grouped_masked_silu_mul_quant")
+    return out, out_scale
 
 
 def device_error(device: int = None) -> int:

@@ -242,11 +242,11 @@ int launch(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensor
 
 // CTA-pair kernel: cluster of 2, persistent over at most the number of pairs
 // that fit on the device at once.
-template <typename OutT, bool kMasked>
+template <typename OutT, bool kMasked, bool kSwiglu = false>
 int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensorMap& tb,
                 const GemmParams& p, int64_t units_bound, cudaStream_t stream) {
     using L = fp8bs::PairLayout;
-    auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, kMasked>;
+    auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, kMasked, kSwiglu>;
     const int smem = L::kBytes + L::kAlignSlack;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -386,7 +386,7 @@ int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUte
                         const CUtensorMap& tb, GemmParams q, int64_t units_bound,
                         cudaStream_t stream) {
     using L = fp8bs::PairLayout;
-    auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, false>;
+    auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, false, false>;
     const int smem = L::kBytes + L::kAlignSlack;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -589,6 +589,139 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     const int64_t tiles = num_groups * p.num_m_tiles * p.num_n_tiles;
     return dispatch<true>(*st, bn, out_dtype, *ta, *tb, p, tiles,
                           static_cast<cudaStream_t>(stream));
+}
+
+// Output scales of the fused gate/up epilogue: [rows, n/256] (MK) or the
+// transposed [n/256, ld] (KM), the two activation-scale layouts the grouped
+// GEMM itself accepts, so the result feeds the down projection directly.
+static int validate_out_scale(const float* out_scale, int layout, int64_t ld, int64_t rows) {
+    if (!out_scale || !aligned(out_scale, 4)) return FP8BS_ERR_INVALID_ARG;
+    if (layout == FP8BS_SA_MK) return FP8BS_OK;
+    if (layout != FP8BS_SA_KM) return FP8BS_ERR_INVALID_ARG;
+    if (ld < rows || ld % 4 || !aligned(out_scale, 16)) return FP8BS_ERR_INVALID_ARG;
+    return FP8BS_OK;
+}
+
+int gemm_grouped_contiguous_silu_mul_quant(const void* a, const float* scale_a, int sa_layout,
+                                           int64_t ld_sa, const void* b, const float* scale_b,
+                                           const int32_t* grouped_layout, void* out,
+                                           float* out_scale, int out_scale_layout,
+                                           int64_t ld_out_scale, int64_t m_sum, int64_t n,
+                                           int64_t k, int64_t num_groups, void* stream) {
+    if (m_sum < 0 || m_sum > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (n <= 0 || k <= 0 || n % 256 || k % 128 || num_groups < 1) return FP8BS_ERR_INVALID_ARG;
+    if ((sa_layout != FP8BS_SA_MK && sa_layout != FP8BS_SA_KM) ||
+        (out_scale_layout != FP8BS_SA_MK && out_scale_layout != FP8BS_SA_KM))
+        return FP8BS_ERR_INVALID_ARG;
+    if (m_sum == 0) return FP8BS_OK;
+    int v = validate_common(a, scale_a, sa_layout, ld_sa, b, scale_b, out, FP8BS_OUT_BF16, m_sum,
+                            n, k, num_groups);
+    if (v != FP8BS_OK) return v;
+    if ((v = validate_out_scale(out_scale, out_scale_layout, ld_out_scale, m_sum)) != FP8BS_OK)
+        return v;
+    if (!grouped_layout || !aligned(grouped_layout, 4) || !aligned(out, 32))
+        return FP8BS_ERR_INVALID_ARG;
+    const int64_t m_tiles = (m_sum + 127) / 128;
+    if (m_tiles > fp8bs::kPairMaxTiles || num_groups >= (1 << 18)) return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const CUtensorMap *ta = nullptr, *tb = nullptr;
+    constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
+    if ((rc = get_map3(dev, a, k, m_sum, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
+    if ((rc = get_map3(dev, b, k, num_groups * n, 128, kKbBox, &tb)) != FP8BS_OK) return rc;
+
+    GemmParams p{};
+    p.sa = scale_a;
+    p.sb = scale_b;
+    p.row_info = grouped_layout;
+    p.d = out;
+    p.err = st->err;
+    p.rows = m_sum;
+    p.sa_g_stride = 0;
+    p.sa_kb_stride = sa_layout == FP8BS_SA_KM ? ld_sa : 1;
+    p.sa_row_stride = sa_layout == FP8BS_SA_KM ? 1 : k / 128;
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(k / 128);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>(m_tiles);
+    p.num_n_tiles = static_cast<int>(n / 256);  // 128-column output blocks
+    p.raster_band = 8;
+    p.q_scale = out_scale;
+    p.qs_g_stride = 0;
+    p.qs_row_stride = out_scale_layout == FP8BS_SA_KM ? 1 : n / 256;
+    p.qs_col_stride = out_scale_layout == FP8BS_SA_KM ? ld_out_scale : 1;
+    return launch_pair<__nv_bfloat16, false, true>(*st, 24, *ta, *tb, p,
+                                                   m_tiles * p.num_n_tiles,
+                                                   static_cast<cudaStream_t>(stream));
+}
+
+int gemm_grouped_masked_silu_mul_quant(const void* a, const float* scale_a, int sa_layout,
+                                       int64_t ld_sa, const void* b, const float* scale_b,
+                                       const int32_t* masked_m, int64_t expected_m, void* out,
+                                       float* out_scale, int out_scale_layout,
+                                       int64_t ld_out_scale, int64_t num_groups, int64_t m_max,
+                                       int64_t n, int64_t k, void* stream) {
+    (void)expected_m;  // scheduling hint only; results never depend on it
+    if (m_max < 0 || num_groups < 1 || num_groups > fp8bs::kMaxMaskedGroups)
+        return FP8BS_ERR_INVALID_ARG;
+    if (m_max > 0 && num_groups * m_max > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (n <= 0 || k <= 0 || n % 256 || k % 128) return FP8BS_ERR_INVALID_ARG;
+    if ((sa_layout != FP8BS_SA_MK && sa_layout != FP8BS_SA_KM) ||
+        (out_scale_layout != FP8BS_SA_MK && out_scale_layout != FP8BS_SA_KM))
+        return FP8BS_ERR_INVALID_ARG;
+    if (m_max == 0) return FP8BS_OK;
+    int v = validate_common(a, scale_a, sa_layout, ld_sa, b, scale_b, out, FP8BS_OUT_BF16, m_max,
+                            n, k, num_groups);
+    if (v != FP8BS_OK) return v;
+    if ((v = validate_out_scale(out_scale, out_scale_layout, ld_out_scale, m_max)) != FP8BS_OK)
+        return v;
+    if (!masked_m || !aligned(masked_m, 4) || !aligned(out, 32)) return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const CUtensorMap *ta = nullptr, *tb = nullptr;
+    constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
+    if ((rc = get_map3(dev, a, k, num_groups * m_max, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
+    if ((rc = get_map3(dev, b, k, num_groups * n, 128, kKbBox, &tb)) != FP8BS_OK) return rc;
+
+    const int64_t kb = k / 128;
+    const int64_t blocks = n / 256;
+    GemmParams p{};
+    p.sa = scale_a;
+    p.sb = scale_b;
+    p.row_info = masked_m;
+    p.d = out;
+    p.err = st->err;
+    p.rows = m_max;
+    p.sa_g_stride = sa_layout == FP8BS_SA_KM ? kb * ld_sa : m_max * kb;
+    p.sa_kb_stride = sa_layout == FP8BS_SA_KM ? ld_sa : 1;
+    p.sa_row_stride = sa_layout == FP8BS_SA_KM ? 1 : kb;
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(kb);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>((m_max + 127) / 128);
+    p.num_n_tiles = static_cast<int>(blocks);
+    p.raster_band = 1;
+    p.q_scale = out_scale;
+    p.qs_g_stride = out_scale_layout == FP8BS_SA_KM ? blocks * ld_out_scale : m_max * blocks;
+    p.qs_row_stride = out_scale_layout == FP8BS_SA_KM ? 1 : blocks;
+    p.qs_col_stride = out_scale_layout == FP8BS_SA_KM ? ld_out_scale : 1;
+    const int64_t units = num_groups * ((m_max + 255) / 256) * blocks;
+    return launch_pair<__nv_bfloat16, true, true>(*st, 25, *ta, *tb, p, units,
+                                                  static_cast<cudaStream_t>(stream));
 }
 
 // Contiguous grouped GEMM that allocates nothing: the CTA-pair kernel with its

@@ -66,6 +66,12 @@ struct GemmParams {
     float* sk_partial;           // sk_slots x [128 rows x 256 cols] fp32 partial accumulators
     uint32_t* sk_flags;          // 2 words per slot (ready tail warps; spare), 0 between launches
     int sk_slots;                // slots available (needs 2 per CTA pair of the grid)
+    // fused gate/up epilogue of the CTA-pair kernel: d receives E4M3 codes [rows, n/2],
+    // q_scale one fp32 UE8M0 scale per row and 128-column block
+    float* q_scale;
+    int64_t qs_g_stride;         // masked: elements between groups; contiguous: 0
+    int64_t qs_row_stride;       // elements between rows
+    int64_t qs_col_stride;       // elements between 128-column blocks
 };
 
 template <int BN>

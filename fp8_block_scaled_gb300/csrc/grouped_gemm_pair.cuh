@@ -49,6 +49,19 @@
 //           synchronous with the tensor pipe, so this thread does nothing
 //           between MMAs but one barrier wait and the scale copies.
 //   warps 4-7 epilogue of the CTA's own 128 rows
+//
+// Fused gate/up epilogue (kSwiglu): for the first MoE GEMM, whose B holds the
+// gate rows [0, N/2) and the up rows [N/2, N) of each expert, a unit covers
+// 128 output columns j0..j0+127: the leader CTA loads gate rows j0.., the peer
+// up rows N/2+j0.., so each CTA's accumulator holds gate in columns 0-127 and
+// up in 128-255 for its 128 rows.  Each epilogue thread owns one row: it forms
+// h = SiLU(gate) * up for the 128 columns ("flydsl mxfp4 a4w4 MoE: bring
+// gemm1/gemm2 to parity with the HIP backend", section gemm1, silu_mul with
+// the hardware exponential), takes the block's amax, the UE8M0 ceil scale of
+// amax / 448 and the round-to-nearest-even E4M3 codes of h / scale (the
+// quantiser of "Adds Grouped and Batched GEMM kernels with blockscaling
+// matching DeepGEMM API", DeepGEMM conformance details), and stores 128 code
+// bytes and one fp32 scale: the input format of the down projection.
 #pragma once
 
 #include "grouped_gemm.cuh"
@@ -100,6 +113,49 @@ struct PairLayout {
 // part of the pair" flag (bit 12), expert id (bits 13..31).
 __device__ __forceinline__ uint32_t pack_pair(int t0, bool half, int g) {
     return static_cast<uint32_t>(t0) | (half ? 1u << 12 : 0u) | (static_cast<uint32_t>(g) << 13);
+}
+
+// SiLU with the hardware exponential and the approximate (reciprocal-based)
+// division: a relative error of a few fp32 ulps, far below one E4M3 step.  The
+// IEEE-rounded division doubled the fused kernel's time.  Below x = -87 the
+// denominator exceeds 2^126 and the quotient is a signed zero (the exact value
+// is below 1e-35 in magnitude).
+__device__ __forceinline__ float silu_f32(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+// Four fp32 values -> four E4M3 codes (round to nearest even, finite values
+// saturated), x0 in the lowest byte.  cvt ...e4m3x2 puts its first source in
+// the upper byte of the 16-bit result.
+__device__ __forceinline__ uint32_t pack4_e4m3(float x0, float x1, float x2, float x3) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// One row's 128 activations -> UE8M0 ceil scale of amax / 448 (amax at least
+// 1e-4, so an all-zero block gets a finite scale) and E4M3 codes of h / scale.
+// The scale is a power of two, so h * (1 / scale) is exact.
+__device__ __forceinline__ void quantize_store_row(const float (&h)[128], uint8_t* qdst,
+                                                   float* sdst, bool valid) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 128; ++i) amax = fmaxf(amax, fabsf(h[i]));
+    amax = fmaxf(amax, 1e-4f);
+    const uint32_t tb = __float_as_uint(__fdiv_rn(amax, 448.0f));
+    const uint32_t e = ((tb >> 23) & 0xFFu) + ((tb & 0x7FFFFFu) != 0u ? 1u : 0u);
+    const float inv = __uint_as_float((254u - e) << 23);
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        w[i] = pack4_e4m3(h[4 * i] * inv, h[4 * i + 1] * inv, h[4 * i + 2] * inv,
+                          h[4 * i + 3] * inv);
+    if (valid) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            st_global_v8(qdst + 32 * i, w[8 * i], w[8 * i + 1], w[8 * i + 2], w[8 * i + 3],
+                         w[8 * i + 4], w[8 * i + 5], w[8 * i + 6], w[8 * i + 7]);
+        *sdst = __uint_as_float(e << 23);
+    }
 }
 
 // Block-wide scans over one int per thread (256 threads); scratch holds 16 ints.
@@ -182,7 +238,7 @@ struct PairUnit {
     bool store;   // this CTA's half belongs to the unit
 };
 
-template <typename OutT, bool kMasked>
+template <typename OutT, bool kMasked, bool kSwiglu>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
@@ -422,7 +478,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     auto unit_rows = [&](const PairUnit& w, int64_t* a_row0, int* b_row0) {
         *a_row0 = kMasked ? static_cast<int64_t>(w.g) * p.rows + w.m_base
                           : static_cast<int64_t>(w.m_base);
-        *b_row0 = w.g * p.n + w.n_tile * 256 + static_cast<int>(rank) * 128;
+        // fused gate/up: the leader holds gate rows, the peer the matching up rows
+        *b_row0 = kSwiglu ? w.g * p.n + static_cast<int>(rank) * (p.n >> 1) + w.n_tile * 128
+                          : w.g * p.n + w.n_tile * 256 + static_cast<int>(rank) * 128;
     };
 
     if (warp == 0 || warp == 2) {
@@ -493,8 +551,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         }
                         if (lane < 2) {
                             const bool in = kb < KB;
+                            // the two 128-column chunks of the unit's B tile
+                            const int nb = kSwiglu ? lane * (p.n >> 8) + w.n_tile : nb0 + lane;
                             const float* src =
-                                p.sb + (static_cast<int64_t>(w.g) * p.nb_count + nb0 + lane) * KB + kb;
+                                p.sb + (static_cast<int64_t>(w.g) * p.nb_count + nb) * KB + kb;
                             cp_async_4(sbase + L::kOffSbRaw + (s * L::kKbPerStage + j) * L::kSbRawBytes +
                                            4u * lane,
                                        in ? src : p.sb, in ? 4u : 0u);
@@ -642,7 +702,26 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
             uint8_t* dst = reinterpret_cast<uint8_t*>(static_cast<OutT*>(p.d) + drow * p.n +
                                                       w.n_tile * 256);
-            if (pc.kind == 0) {
+            // fused gate/up: 128 code bytes of this row and its scale for the unit's block
+            uint8_t* qdst = reinterpret_cast<uint8_t*>(p.d) + drow * (p.n >> 1) + w.n_tile * 128;
+            float* sdst = p.q_scale + (kMasked ? static_cast<int64_t>(w.g) * p.qs_g_stride : 0) +
+                          m * p.qs_row_stride + w.n_tile * p.qs_col_stride;
+            if (kSwiglu && pc.kind == 0) {
+                float h[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {  // 32 gate columns and the matching up columns
+                    uint32_t gv[32], uv[32];
+                    tc_ld_32x32b_x32_sync(trow + 32 * c, gv);
+                    tc_ld_32x32b_x32_sync(trow + 128 + 32 * c, uv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        h[32 * c + i] = silu_f32(__uint_as_float(gv[i])) * __uint_as_float(uv[i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
+                quantize_store_row(h, qdst, sdst, valid);
+            } else if (pc.kind == 0) {
                 // the whole 256-column row goes to registers as packed bf16/f16 pairs
                 // first, so the accumulator is handed back before any global store
                 uint32_t packed[4][32];
@@ -722,8 +801,52 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                   bar_part(c));
                     }
                 }
+                if constexpr (kSwiglu) {
+                    // partial column col of this row in the staged slot: chunk col / 64,
+                    // column group (col % 64) / 8, [128 rows][8 columns] per group
+                    const float* part = reinterpret_cast<const float*>(smem + L::kOffA) + row_in_half * 8;
+                    float h[128];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {  // 32 gate columns and the matching up columns
+                        uint32_t gv[32], uv[32];
+                        tc_ld_32x32b_x32_sync(trow + 32 * c, gv);
+                        tc_ld_32x32b_x32_sync(trow + 128 + 32 * c, uv);
+                        if (c == 3) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
+                        }
+                        if ((c & 1) == 0) {  // gate chunk c/2 and up chunk 2 + c/2
+                            if (!pair_warp_wait(bar_part(c >> 1), 0, abort_flag, peer_abort, p.err) ||
+                                !pair_warp_wait(bar_part(2 + (c >> 1)), 0, abort_flag, peer_abort,
+                                                p.err)) {
+                                aborted = true;
+                                break;
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const int gcol = 32 * c + i, ucol = 128 + 32 * c + i;
+                            const float4 gp = *reinterpret_cast<const float4*>(
+                                part + (gcol >> 6) * (L::kPartChunkBytes / 4) +
+                                ((gcol & 63) >> 3) * (128 * 8) + (gcol & 7));
+                            const float4 up = *reinterpret_cast<const float4*>(
+                                part + (ucol >> 6) * (L::kPartChunkBytes / 4) +
+                                ((ucol & 63) >> 3) * (128 * 8) + (ucol & 7));
+                            h[32 * c + i] = silu_f32(__uint_as_float(gv[i]) + gp.x) *
+                                            (__uint_as_float(uv[i]) + up.x);
+                            h[32 * c + i + 1] = silu_f32(__uint_as_float(gv[i + 1]) + gp.y) *
+                                                (__uint_as_float(uv[i + 1]) + up.y);
+                            h[32 * c + i + 2] = silu_f32(__uint_as_float(gv[i + 2]) + gp.z) *
+                                                (__uint_as_float(uv[i + 2]) + up.z);
+                            h[32 * c + i + 3] = silu_f32(__uint_as_float(gv[i + 3]) + gp.w) *
+                                                (__uint_as_float(uv[i + 3]) + up.w);
+                        }
+                    }
+                    if (!aborted) quantize_store_row(h, qdst, sdst, valid);
+                }
 #pragma unroll 1
-                for (int c = 0; c < L::kPartChunks; ++c) {
+                for (int c = 0; c < (kSwiglu ? 0 : L::kPartChunks); ++c) {
                     uint32_t v[64];
                     tc_ld_32x32b_x64_sync(trow + c * 64, v);
                     if (c == 3) {

@@ -126,6 +126,66 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
                         int64_t m_max, int64_t n, int64_t k, void* stream);
 
 /*
+ * Fused first MoE GEMM: the grouped GEMM of the gate/up projection followed by
+ * SiLU(gate) * up and requantisation for the down projection.
+ *   - silu_mul of the gate and up halves: "flydsl mxfp4 a4w4 MoE: bring
+ *     gemm1/gemm2 to parity with the HIP backend" (aiter PR #3828), section
+ *     gemm1 (the exponential is the hardware one, __expf);
+ *   - the quantiser of the activations of "Adds Grouped and Batched GEMM
+ *     kernels with blockscaling matching DeepGEMM API", DeepGEMM conformance
+ *     details: per (1,128) block, scale = smallest power of two >= amax / 448
+ *     (amax at least 1e-4), codes = E4M3 round-to-nearest-even of h / scale.
+ *
+ * For each computed row r of expert g and output column j < n/2:
+ *     gate = acc(r, j), up = acc(r, n/2 + j), with acc the block-scaled product
+ *            of gemm_grouped_contiguous against B[g] (rows [0, n/2) of each
+ *            expert's B are the gate projection, rows [n/2, n) the up one);
+ *     h    = gate / (1 + exp(-gate)) * up, in fp32;
+ *     out[r, j] = E4M3(h / out_scale[r, j/128]).
+ * The scale exponent and the codes are decided in fp32 from the fp32
+ * accumulator, so a code whose exact value lies within a few fp32 ulps of an
+ * E4M3 rounding boundary (or a scale whose amax / 448 lies that close to a
+ * power of two) may come out as either neighbour.
+ *
+ *   a, scale_a, sa_layout, ld_sa, b, scale_b, grouped_layout: as for
+ *              gemm_grouped_contiguous, with n = 2 * (output columns)
+ *   out        E4M3 [m_sum, n/2], 32-byte aligned
+ *   out_scale  fp32, out_scale_layout FP8BS_SA_MK: [m_sum, n/256];
+ *              FP8BS_SA_KM: [n/256, ld_out_scale], ld_out_scale >= m_sum,
+ *              ld_out_scale % 4 == 0, 16-byte aligned.  Either is a scale_a
+ *              layout of gemm_grouped_contiguous, so (out, out_scale) is the
+ *              activation operand of the down projection as it stands.
+ *   n % 256 == 0 (n/2 a multiple of 128), m_sum <= 524288, num_groups < 2^18:
+ *              the op runs on the CTA-pair kernel only; other shapes return
+ *              FP8BS_ERR_INVALID_ARG.
+ * Rows with grouped_layout == -1 are written neither in out nor in out_scale.
+ * Scratch as for gemm_grouped_contiguous (the per-stream stream-K workspace).
+ */
+int gemm_grouped_contiguous_silu_mul_quant(const void* a, const float* scale_a, int sa_layout,
+                                           int64_t ld_sa, const void* b, const float* scale_b,
+                                           const int32_t* grouped_layout, void* out,
+                                           float* out_scale, int out_scale_layout,
+                                           int64_t ld_out_scale, int64_t m_sum, int64_t n,
+                                           int64_t k, int64_t num_groups, void* stream);
+
+/*
+ * Masked variant of gemm_grouped_contiguous_silu_mul_quant (the decode-time
+ * layout of gemm_grouped_masked): group g computes its first masked_m[g] rows.
+ *   out        E4M3 [num_groups, m_max, n/2], 32-byte aligned
+ *   out_scale  fp32, FP8BS_SA_MK: [num_groups, m_max, n/256];
+ *              FP8BS_SA_KM: [num_groups, n/256, ld_out_scale],
+ *              ld_out_scale >= m_max, ld_out_scale % 4 == 0, 16-byte aligned
+ *   other arguments as for gemm_grouped_masked, with n % 256 == 0.
+ * Rows m >= masked_m[g] are written neither in out nor in out_scale.
+ */
+int gemm_grouped_masked_silu_mul_quant(const void* a, const float* scale_a, int sa_layout,
+                                       int64_t ld_sa, const void* b, const float* scale_b,
+                                       const int32_t* masked_m, int64_t expected_m, void* out,
+                                       float* out_scale, int out_scale_layout,
+                                       int64_t ld_out_scale, int64_t num_groups, int64_t m_max,
+                                       int64_t n, int64_t k, void* stream);
+
+/*
  * Contiguous grouped GEMM that allocates no device memory.  (No counterpart on
  * the pages: an addition for callers that may not call cudaMalloc -- for
  * example code that runs under a memory pool or allocator that owns all device

@@ -56,6 +56,13 @@ CONFIGS: Dict[str, dict] = {
     "c6_dense_g1_m4096_n4096_k16384": dict(
         variant="contiguous", G=1, N=4096, K=16384, out=OUT_BF16, sa_layout=SA_MK,
         sizes=("fixed", 4096), seed=6),
+    # the first MoE GEMM with its fused epilogue: B holds each expert's gate rows
+    # [0, 2048) and up rows [2048, 4096) (DeepSeek-V3 expert shape, hidden 7168,
+    # intermediate 2048); the output is SiLU(gate) * up requantised to E4M3 with
+    # (1,128) UE8M0 scales in the activation-scale layout named by sa_layout
+    "c7_swiglu_contig_g8_m1024_n4096_k7168": dict(
+        variant="contiguous", G=8, N=4096, K=7168, out=OUT_BF16, sa_layout=SA_KM,
+        sizes=("fixed", 1024), seed=7, epilogue="silu_mul_quant"),
 }
 
 
@@ -151,6 +158,7 @@ class Problem:
     M_max: int = 0
     row_offsets: Optional[List[int]] = None        # contiguous: first row of each group
     pad_multiple: int = 128
+    epilogue: str = ""    # "" (bf16/f16 D) or "silu_mul_quant" (E4M3 codes + scales of SiLU(gate)*up)
 
     @property
     def KB(self) -> int:
@@ -176,6 +184,9 @@ class Problem:
         sa = self.valid_rows * self.KB * 4
         sb = used * (self.N // 128) * self.KB * 4
         d = self.valid_rows * self.N * out_bytes
+        if self.epilogue == "silu_mul_quant":
+            # N/2 code bytes and N/256 fp32 scales per row
+            d = self.valid_rows * (self.N // 2 + (self.N // 256) * 4)
         rowmap = self.a.shape[0] * 4 if self.variant == "contiguous" else self.G * 4
         return float(a + b + sa + sb + d + rowmap)
 
@@ -299,9 +310,11 @@ def make_config(name: str, device="cpu") -> Problem:
     """One of the named workloads of CONFIGS."""
     c = CONFIGS[name]
     sizes = draw_group_sizes(c["sizes"], c["G"], c["seed"])
-    return make_problem(c["variant"], c["G"], c["N"], c["K"], sizes, out_dtype=c["out"],
-                        sa_layout=c["sa_layout"], seed=c["seed"], M_max=c.get("M_max", 0),
-                        device=device, name=name)
+    p = make_problem(c["variant"], c["G"], c["N"], c["K"], sizes, out_dtype=c["out"],
+                     sa_layout=c["sa_layout"], seed=c["seed"], M_max=c.get("M_max", 0),
+                     device=device, name=name)
+    p.epilogue = c.get("epilogue", "")
+    return p
 
 
 def sample_rows(p: Problem, per_group: int = 32, seed: int = 0):

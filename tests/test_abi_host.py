@@ -142,3 +142,51 @@ def test_noalloc_rejects(lib, bad):
 def test_noalloc_empty_is_noop(lib):
     assert _noalloc(m_sum=0, a=0) == OK
 
+
+
+def _fused(**kw):
+    args = dict(a=P, sa=P, sa_layout=0, ld_sa=0, b=P, sb=P, lay=P, out=P, os=P, osl=0, ldo=0,
+                m_sum=256, n=512, k=256, g=2)
+    args.update(kw)
+    return _binding.gemm_grouped_contiguous_silu_mul_quant_raw(
+        args["a"], args["sa"], args["sa_layout"], args["ld_sa"], args["b"], args["sb"],
+        args["lay"], args["out"], args["os"], args["osl"], args["ldo"], args["m_sum"], args["n"],
+        args["k"], args["g"], 0)
+
+
+def _fused_masked(**kw):
+    args = dict(a=P, sa=P, sa_layout=0, ld_sa=0, b=P, sb=P, mm=P, out=P, os=P, osl=0, ldo=0,
+                g=2, m_max=64, n=512, k=256)
+    args.update(kw)
+    return _binding.gemm_grouped_masked_silu_mul_quant_raw(
+        args["a"], args["sa"], args["sa_layout"], args["ld_sa"], args["b"], args["sb"],
+        args["mm"], 0, args["out"], args["os"], args["osl"], args["ldo"], args["g"],
+        args["m_max"], args["n"], args["k"], 0)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n=384),                 # n/2 must be a multiple of 128
+    dict(n=128),
+    dict(out=P + 16),            # codes are stored 32 bytes at a time
+    dict(os=0), dict(os=P + 2), dict(osl=2),
+    dict(osl=1, ldo=255), dict(osl=1, ldo=258), dict(osl=1, ldo=256, os=P + 4),
+    dict(m_sum=524288 + 128),    # pair-list limit
+    dict(g=1 << 18),
+    dict(a=0), dict(lay=0), dict(k=100), dict(sa_layout=5),
+])
+def test_fused_contiguous_rejects(lib, bad):
+    assert _fused(**bad) == INVALID
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n=384), dict(out=P + 16), dict(os=0), dict(osl=1, ldo=63), dict(osl=1, ldo=66),
+    dict(mm=0), dict(g=0), dict(g=1025), dict(m_max=-1),
+])
+def test_fused_masked_rejects(lib, bad):
+    assert _fused_masked(**bad) == INVALID
+
+
+def test_fused_empty_is_noop(lib):
+    assert _fused(m_sum=0, a=0, out=0, os=0) == OK
+    assert _fused_masked(m_max=0, a=0, out=0, os=0) == OK
+    assert _fused(m_sum=0, n=384) == INVALID

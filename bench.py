@@ -195,6 +195,11 @@ def run_once(fb, p, a, sa, b, sb, rowinfo, d, stream=None):
             fb.gemm_grouped_contiguous_silu_mul_quant(a, sa, b, sb, q, qs, rowinfo, stream=stream)
         else:
             fb.gemm_grouped_masked_silu_mul_quant(a, sa, b, sb, q, qs, rowinfo, stream=stream)
+    elif p.scale_kind == "fp32":
+        if p.variant == "contiguous":
+            fb.gemm_grouped_contiguous_fp32_scales(a, sa, b, sb, d, rowinfo, stream=stream)
+        else:
+            fb.gemm_grouped_masked_fp32_scales(a, sa, b, sb, d, rowinfo, stream=stream)
     elif p.variant == "contiguous":
         fb.gemm_grouped_contiguous(a, sa, b, sb, d, rowinfo, stream=stream)
     else:
@@ -232,7 +237,9 @@ def describe(p, l2_note):
            "valid_rows": p.valid_rows, "rows": p.rows,
            "out": "bf16" if p.out_dtype == 0 else "f16",
            "scale_a": "transposed [K/128, M]" if p.sa_layout == 1 else "[M, K/128]",
-           "scales": "UE8M0 (1,128) activation x (128,128) weight",
+           "scales": ("UE8M0 (1,128) activation x (128,128) weight" if p.scale_kind == "ue8m0"
+                      else "arbitrary fp32 (1,128) activation x (128,128) weight, promoted in "
+                           "software"),
            "parallelism": "replicas (no exchange step)", "l2": l2_note}
     if p.variant == "masked":
         cfg["M_max"] = p.M_max

@@ -11,7 +11,9 @@ accumulation, bf16/f16 output, in a contiguous (grouped_layout, -1 = padding)
 and a masked (masked_m) variant.  All compute runs in the hand-written CUDA
 kernels of ``libfp8bs.so``; this package only marshals arguments.  The
 ``*_silu_mul_quant`` entry points fuse the first MoE GEMM's SiLU(gate) * up and
-the (1,128) E4M3 requantisation of its output into the same kernel.
+the (1,128) E4M3 requantisation of its output into the same kernel; the
+``*_fp32_scales`` entry points take arbitrary fp32 block scales (promoted in
+software instead of by the tensor core).
 """
 from ._binding import (  # noqa: F401
     DEVERR_BAD_GROUP,
@@ -28,11 +30,15 @@ from ._binding import (  # noqa: F401
     clear_cache,
     device_error,
     gemm_grouped_contiguous,
+    gemm_grouped_contiguous_fp32_scales,
+    gemm_grouped_contiguous_fp32_scales_raw,
     gemm_grouped_contiguous_noalloc_raw,
     gemm_grouped_contiguous_raw,
     gemm_grouped_contiguous_silu_mul_quant,
     gemm_grouped_contiguous_silu_mul_quant_raw,
     gemm_grouped_masked,
+    gemm_grouped_masked_fp32_scales,
+    gemm_grouped_masked_fp32_scales_raw,
     gemm_grouped_masked_raw,
     gemm_grouped_masked_silu_mul_quant,
     gemm_grouped_masked_silu_mul_quant_raw,

@@ -30,6 +30,7 @@ DEVERR_BAD_GROUP = 0x8
 # every symbol include/fp8bs.h declares
 EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "gemm_grouped_contiguous_noalloc",
            "gemm_grouped_contiguous_silu_mul_quant", "gemm_grouped_masked_silu_mul_quant",
+           "gemm_grouped_contiguous_fp32_scales", "gemm_grouped_masked_fp32_scales",
            "fp8bs_device_error", "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version")
 
 _lib = None
@@ -75,6 +76,10 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.gemm_grouped_masked_silu_mul_quant.argtypes = [_P, _P, _I, _I64, _P, _P, _P, _I64, _P,
                                                            _P, _I, _I64, _I64, _I64, _I64, _I64, _P]
         lib.gemm_grouped_masked_silu_mul_quant.restype = _I
+        lib.gemm_grouped_contiguous_fp32_scales.argtypes = lib.gemm_grouped_contiguous.argtypes
+        lib.gemm_grouped_contiguous_fp32_scales.restype = _I
+        lib.gemm_grouped_masked_fp32_scales.argtypes = lib.gemm_grouped_masked.argtypes
+        lib.gemm_grouped_masked_fp32_scales.restype = _I
         lib.fp8bs_device_error.argtypes = [_I, ctypes.POINTER(ctypes.c_uint32)]
         lib.fp8bs_device_error.restype = _I
         lib.fp8bs_status_string.argtypes = [_I]
@@ -174,7 +179,42 @@ def gemm_grouped_masked_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr, mask
                                    ctypes.c_void_p(_stream_handle(stream)))
 
 
-def gemm_grouped_contiguous(a, scale_a, b, scale_b, d, grouped_layout, *, stream=None):
+def gemm_grouped_contiguous_fp32_scales_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr,
+                                            layout_ptr, d_ptr, out_dtype, m_sum, n, k,
+                                            num_groups, stream=None) -> int:
+    lib = load()
+    return lib.gemm_grouped_contiguous_fp32_scales(
+        a_ptr, sa_ptr, int(sa_layout), int(ld_sa), b_ptr, sb_ptr, layout_ptr, d_ptr,
+        int(out_dtype), int(m_sum), int(n), int(k), int(num_groups),
+        ctypes.c_void_p(_stream_handle(stream)))
+
+
+def gemm_grouped_masked_fp32_scales_raw(a_ptr, sa_ptr, sa_layout, ld_sa, b_ptr, sb_ptr,
+                                        masked_m_ptr, expected_m, d_ptr, out_dtype, num_groups,
+                                        m_max, n, k, stream=None) -> int:
+    lib = load()
+    return lib.gemm_grouped_masked_fp32_scales(
+        a_ptr, sa_ptr, int(sa_layout), int(ld_sa), b_ptr, sb_ptr, masked_m_ptr, int(expected_m),
+        d_ptr, int(out_dtype), int(num_groups), int(m_max), int(n), int(k),
+        ctypes.c_void_p(_stream_handle(stream)))
+
+
+def gemm_grouped_contiguous_fp32_scales(a, scale_a, b, scale_b, d, grouped_layout, *,
+                                        stream=None):
+    """As gemm_grouped_contiguous, with arbitrary fp32 block scales (software promotion)."""
+    return gemm_grouped_contiguous(a, scale_a, b, scale_b, d, grouped_layout, stream=stream,
+                                   _raw=gemm_grouped_contiguous_fp32_scales_raw)
+
+
+def gemm_grouped_masked_fp32_scales(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0, *,
+                                    stream=None):
+    """As gemm_grouped_masked, with arbitrary fp32 block scales (software promotion)."""
+    return gemm_grouped_masked(a, scale_a, b, scale_b, d, masked_m, expected_m, stream=stream,
+                               _raw=gemm_grouped_masked_fp32_scales_raw)
+
+
+def gemm_grouped_contiguous(a, scale_a, b, scale_b, d, grouped_layout, *, stream=None,
+                            _raw=None):
     """D = grouped FP8 block-scaled GEMM, contiguous variant (see include/fp8bs.h).
 
     a [M_sum, K] e4m3; scale_a logical [M_sum, K/128] fp32 (row-major, or a
@@ -194,16 +234,16 @@ def gemm_grouped_contiguous(a, scale_a, b, scale_b, d, grouped_layout, *, stream
         if not t.is_cuda:
             raise ValueError("all tensors must be CUDA tensors")
     layout, ld = _sa_layout_2d(scale_a, m_sum, k // 128)
-    st = gemm_grouped_contiguous_raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld,
-                                     _fp8_ptr(b, "b"), scale_b.contiguous().data_ptr(),
-                                     grouped_layout.contiguous().data_ptr(), d.data_ptr(),
-                                     _out_code(d), m_sum, n, k, G, stream)
-    _check(st, "gemm_grouped_contiguous")
+    raw = _raw or gemm_grouped_contiguous_raw
+    st = raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
+             scale_b.contiguous().data_ptr(), grouped_layout.contiguous().data_ptr(), d.data_ptr(),
+             _out_code(d), m_sum, n, k, G, stream)
+    _check(st, raw.__name__[:-4])
     return d
 
 
 def gemm_grouped_masked(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0, *,
-                        stream=None):
+                        stream=None, _raw=None):
     """D = grouped FP8 block-scaled GEMM, masked variant (see include/fp8bs.h).
 
     a [G, M_max, K] e4m3; scale_a logical [G, M_max, K/128] fp32 (row-major,
@@ -223,11 +263,11 @@ def gemm_grouped_masked(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0
         if not t.is_cuda:
             raise ValueError("all tensors must be CUDA tensors")
     layout, ld = _sa_layout_3d(scale_a, G, m_max, k // 128)
-    st = gemm_grouped_masked_raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld,
-                                 _fp8_ptr(b, "b"), scale_b.contiguous().data_ptr(),
-                                 masked_m.contiguous().data_ptr(), expected_m, d.data_ptr(),
-                                 _out_code(d), G, m_max, n, k, stream)
-    _check(st, "gemm_grouped_masked")
+    raw = _raw or gemm_grouped_masked_raw
+    st = raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
+             scale_b.contiguous().data_ptr(), masked_m.contiguous().data_ptr(), expected_m,
+             d.data_ptr(), _out_code(d), G, m_max, n, k, stream)
+    _check(st, raw.__name__[:-4])
     return d
 
 

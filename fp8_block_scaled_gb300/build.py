@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libfp8bs.so")
 SOURCES = ["fp8bs_api.cu"]
-HEADERS = ["ptx.cuh", "grouped_gemm.cuh", "grouped_gemm_pair.cuh"]
+HEADERS = ["ptx.cuh", "grouped_gemm.cuh", "grouped_gemm_pair.cuh", "grouped_gemm_promote.cuh"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

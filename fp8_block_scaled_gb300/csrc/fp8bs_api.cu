@@ -18,6 +18,7 @@
 #include "fp8bs.h"
 #include "grouped_gemm.cuh"
 #include "grouped_gemm_pair.cuh"
+#include "grouped_gemm_promote.cuh"
 
 // Per-device error word written by the kernels (FP8BS_DEVERR_* bits).
 __device__ uint32_t g_fp8bs_error_word;
@@ -290,6 +291,53 @@ int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUt
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
     cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, q) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_OK;
+}
+
+// Software-promotion kernel (arbitrary fp32 scales): cluster of 2, 384 threads,
+// round-robin units, no scratch.
+template <typename OutT, bool kMasked>
+int launch_promote(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensorMap& tb,
+                   const GemmParams& p, int64_t units_bound, cudaStream_t stream) {
+    using L = fp8bs::PromoteLayout;
+    auto kern = fp8bs::grouped_gemm_promote_kernel<OutT, kMasked>;
+    const int smem = L::kBytes + L::kAlignSlack;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    set_pdl(attr[1]);
+    cfg.blockDim = dim3(fp8bs::kPromoteThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
+    if (!st.attr_set[attr_slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        cfg.gridDim = dim3(2 * (st.sms / 2), 1, 1);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters <= 0) {
+            cudaGetLastError();
+            clusters = st.sms / 2;
+        }
+        st.max_clusters[attr_slot] = clusters;
+        st.attr_set[attr_slot] = true;
+    }
+    const int64_t pairs = units_bound < st.max_clusters[attr_slot] ? units_bound
+                                                                   : st.max_clusters[attr_slot];
+    if (pairs <= 0) return FP8BS_OK;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
@@ -722,6 +770,117 @@ int gemm_grouped_masked_silu_mul_quant(const void* a, const float* scale_a, int 
     const int64_t units = num_groups * ((m_max + 255) / 256) * blocks;
     return launch_pair<__nv_bfloat16, true, true>(*st, 25, *ta, *tb, p, units,
                                                   static_cast<cudaStream_t>(stream));
+}
+
+int gemm_grouped_contiguous_fp32_scales(const void* a, const float* scale_a, int sa_layout,
+                                        int64_t ld_sa, const void* b, const float* scale_b,
+                                        const int32_t* grouped_layout, void* d, int out_dtype,
+                                        int64_t m_sum, int64_t n, int64_t k, int64_t num_groups,
+                                        void* stream) {
+    if (m_sum < 0 || m_sum > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (n <= 0 || k <= 0 || n % 256 || k % 128 || num_groups < 1 ||
+        (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16) ||
+        (sa_layout != FP8BS_SA_MK && sa_layout != FP8BS_SA_KM))
+        return FP8BS_ERR_INVALID_ARG;
+    if (m_sum == 0) return FP8BS_OK;
+    int v = validate_common(a, scale_a, sa_layout, ld_sa, b, scale_b, d, out_dtype, m_sum, n, k,
+                            num_groups);
+    if (v != FP8BS_OK) return v;
+    const int64_t m_tiles = (m_sum + 127) / 128;
+    if (!grouped_layout || !aligned(grouped_layout, 4) || !aligned(d, 32) ||
+        m_tiles > fp8bs::kPairMaxTiles || num_groups >= (1 << 18))
+        return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const CUtensorMap *ta = nullptr, *tb = nullptr;
+    constexpr uint32_t kKbBox = fp8bs::PromoteLayout::kKbPerStage;
+    if ((rc = get_map3(dev, a, k, m_sum, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
+    if ((rc = get_map3(dev, b, k, num_groups * n, 128, kKbBox, &tb)) != FP8BS_OK) return rc;
+
+    GemmParams p{};
+    p.sa = scale_a;
+    p.sb = scale_b;
+    p.row_info = grouped_layout;
+    p.d = d;
+    p.err = st->err;
+    p.rows = m_sum;
+    p.sa_g_stride = 0;
+    p.sa_kb_stride = sa_layout == FP8BS_SA_KM ? ld_sa : 1;
+    p.sa_row_stride = sa_layout == FP8BS_SA_KM ? 1 : k / 128;
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(k / 128);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>(m_tiles);
+    p.num_n_tiles = static_cast<int>(n / 256);
+    p.raster_band = 8;
+    const int64_t units = m_tiles * p.num_n_tiles;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return out_dtype == FP8BS_OUT_BF16
+               ? launch_promote<__nv_bfloat16, false>(*st, 26, *ta, *tb, p, units, s)
+               : launch_promote<__half, false>(*st, 27, *ta, *tb, p, units, s);
+}
+
+int gemm_grouped_masked_fp32_scales(const void* a, const float* scale_a, int sa_layout,
+                                    int64_t ld_sa, const void* b, const float* scale_b,
+                                    const int32_t* masked_m, int64_t expected_m, void* d,
+                                    int out_dtype, int64_t num_groups, int64_t m_max, int64_t n,
+                                    int64_t k, void* stream) {
+    (void)expected_m;  // scheduling hint only; results never depend on it
+    if (m_max < 0 || num_groups < 1 || num_groups > fp8bs::kMaxMaskedGroups)
+        return FP8BS_ERR_INVALID_ARG;
+    if (m_max > 0 && num_groups * m_max > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (n <= 0 || k <= 0 || n % 256 || k % 128 ||
+        (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16) ||
+        (sa_layout != FP8BS_SA_MK && sa_layout != FP8BS_SA_KM))
+        return FP8BS_ERR_INVALID_ARG;
+    if (m_max == 0) return FP8BS_OK;
+    int v = validate_common(a, scale_a, sa_layout, ld_sa, b, scale_b, d, out_dtype, m_max, n, k,
+                            num_groups);
+    if (v != FP8BS_OK) return v;
+    if (!masked_m || !aligned(masked_m, 4) || !aligned(d, 32)) return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const CUtensorMap *ta = nullptr, *tb = nullptr;
+    constexpr uint32_t kKbBox = fp8bs::PromoteLayout::kKbPerStage;
+    if ((rc = get_map3(dev, a, k, num_groups * m_max, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
+    if ((rc = get_map3(dev, b, k, num_groups * n, 128, kKbBox, &tb)) != FP8BS_OK) return rc;
+
+    const int64_t kb = k / 128;
+    GemmParams p{};
+    p.sa = scale_a;
+    p.sb = scale_b;
+    p.row_info = masked_m;
+    p.d = d;
+    p.err = st->err;
+    p.rows = m_max;
+    p.sa_g_stride = sa_layout == FP8BS_SA_KM ? kb * ld_sa : m_max * kb;
+    p.sa_kb_stride = sa_layout == FP8BS_SA_KM ? ld_sa : 1;
+    p.sa_row_stride = sa_layout == FP8BS_SA_KM ? 1 : kb;
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(kb);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>((m_max + 127) / 128);
+    p.num_n_tiles = static_cast<int>(n / 256);
+    p.raster_band = 1;
+    const int64_t units = num_groups * ((m_max + 255) / 256) * p.num_n_tiles;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return out_dtype == FP8BS_OUT_BF16
+               ? launch_promote<__nv_bfloat16, true>(*st, 28, *ta, *tb, p, units, s)
+               : launch_promote<__half, true>(*st, 29, *ta, *tb, p, units, s);
 }
 
 // Contiguous grouped GEMM that allocates nothing: the CTA-pair kernel with its

@@ -94,7 +94,7 @@ struct PairLayout {
     static constexpr int kNumBars = 3 * kStages + 3 + kPartChunks;
     static constexpr int kPrefetchStages = 3;  // stages of A/B prefetched into L2 ahead of the ring
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // slot, abort, scan scratch
-    static constexpr int kMiscBytes = 16 + 2 * 8 * 4;
+    static constexpr int kMiscBytes = 16 + 2 * 16 * 4;
     static constexpr int kOffList = (kOffMisc + kMiscBytes + 15) / 16 * 16;
     static constexpr int kListEntries = kPairMaxTiles + 1;
     static constexpr int kBytes = kOffList + kListEntries * 4;
@@ -104,7 +104,6 @@ struct PairLayout {
     static_assert(256 + kStages * kKbPerStage * kSfColsPerKb <= kTmemCols, "TMEM budget");
     static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
     static_assert(kPairMaxTiles * 4 <= kStages * kAStageBytes, "prologue scratch");
-    static_assert(kPairMaxTiles % kThreads == 0, "grouped_layout loads per thread");
     static_assert(kPartChunks * kPartChunkBytes <= kStages * (kAStageBytes + kBStageBytes),
                   "stream-K partial staging");
 };
@@ -158,8 +157,13 @@ __device__ __forceinline__ void quantize_store_row(const float (&h)[128], uint8_
     }
 }
 
-// Block-wide scans over one int per thread (256 threads); scratch holds 16 ints.
+// Block-wide scans over one int per thread of an NW-warp block; scratch holds
+// 2 * kMaxScanWarps ints (the max scan uses the first half, the sum the second).
+constexpr int kMaxScanWarps = 16;
+
+template <int NW>
 __device__ __forceinline__ int block_exclusive_max(int v, int* scratch) {
+    static_assert(NW <= kMaxScanWarps, "scan scratch");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
 #pragma unroll
@@ -177,7 +181,9 @@ __device__ __forceinline__ int block_exclusive_max(int v, int* scratch) {
     return excl;
 }
 
+template <int NW>
 __device__ __forceinline__ int block_exclusive_sum(int v, int* scratch, int* total) {
+    static_assert(NW <= kMaxScanWarps, "scan scratch");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
 #pragma unroll
@@ -185,12 +191,12 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int* scratch, int* tot
         const int o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
     }
-    if (lane == 31) scratch[8 + warp] = incl;
+    if (lane == 31) scratch[kMaxScanWarps + warp] = incl;
     __syncthreads();
     int prev = 0, all = 0;
-    for (int w = 0; w < 8; ++w) {
-        if (w < warp) prev += scratch[8 + w];
-        all += scratch[8 + w];
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) prev += scratch[kMaxScanWarps + w];
+        all += scratch[kMaxScanWarps + w];
     }
     *total = all;
     const int excl = prev + incl - v;
@@ -237,6 +243,139 @@ struct PairUnit {
     int m_base;   // first row of this CTA's half (contiguous: global row; masked: row in group)
     bool store;   // this CTA's half belongs to the unit
 };
+
+// Work units of one launch, the same on every CTA: contiguous -- the pair list
+// (two 128-row tiles of one expert segment per entry, pack_pair format) built
+// from grouped_layout, times the column tiles; masked -- per group
+// ceil(masked_m[g] / 256) row pairs times the column tiles, as an exclusive
+// prefix in list[0..G].  `scratch` is shared memory that is idle during the
+// prologue (kPairMaxTiles ints).  All NT threads of the block call this.
+template <bool kMasked, int NT>
+__device__ __forceinline__ int build_units(const GemmParams& p, uint8_t* scratch_smem, int* list,
+                                           int* scan_scratch) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int total_units;
+    if constexpr (!kMasked) {
+        // ---- pair list: tiles of each expert segment, two by two
+        const int T = p.num_m_tiles;
+        int* E = reinterpret_cast<int*>(scratch_smem);
+        // all of this thread's grouped_layout reads are issued before the first is used
+        constexpr int kLoads = (kPairMaxTiles + NT - 1) / NT;
+        int ev[kLoads];
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j) {
+            const int t = static_cast<int>(threadIdx.x) + j * NT;
+            ev[j] = t < T ? __ldg(p.row_info + static_cast<int64_t>(t) * kBM) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < kLoads; ++j) {
+            const int t = static_cast<int>(threadIdx.x) + j * NT;
+            if (t < T) {
+                int v = ev[j];
+                if (v >= p.num_groups || v < -1) {
+                    raise_error(p.err, kErrBadGroup);
+                    v = -1;
+                }
+                E[t] = v;
+            }
+        }
+        __syncthreads();
+        const int chunk = (T + NT - 1) / NT;
+        const int lo = min(T, static_cast<int>(threadIdx.x) * chunk);
+        const int hi = min(T, lo + chunk);
+        int last_start = -1;
+        for (int t = lo; t < hi; ++t)
+            if (t == 0 || E[t] != E[t - 1]) last_start = t;
+        const int carry = block_exclusive_max<NT / 32>(last_start, scan_scratch);
+        int start = carry, count = 0;
+        for (int t = lo; t < hi; ++t) {
+            if (t == 0 || E[t] != E[t - 1]) start = t;
+            if (E[t] >= 0 && ((t - start) & 1) == 0) ++count;
+        }
+        int total = 0;
+        int idx = block_exclusive_sum<NT / 32>(count, scan_scratch, &total);
+        start = carry;
+        for (int t = lo; t < hi; ++t) {
+            if (t == 0 || E[t] != E[t - 1]) start = t;
+            if (E[t] >= 0 && ((t - start) & 1) == 0) {
+                const bool half = (t + 1 >= T) || (E[t + 1] != E[t]);
+                list[idx++] = static_cast<int>(pack_pair(t, half, E[t]));
+            }
+        }
+        total_units = total * p.num_n_tiles;
+    } else {
+        // ---- masked: pairs per group and their prefix (warp 3)
+        if (warp == 3) {
+            const int G = p.num_groups;
+            const int per = (G + 31) / 32;
+            const int g0 = lane * per;
+            int local = 0;
+            for (int g = g0; g < min(G, g0 + per); ++g) {
+                int mm = __ldg(p.row_info + g);
+                if (mm < 0 || mm > p.rows) {
+                    raise_error(p.err, kErrMaskedM);
+                    mm = mm < 0 ? 0 : static_cast<int>(p.rows);
+                }
+                local += (mm + 2 * kBM - 1) / (2 * kBM) * p.num_n_tiles;
+            }
+            int incl = local;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += v;
+            }
+            int run = incl - local;
+            for (int g = g0; g < min(G, g0 + per); ++g) {
+                list[g] = run;
+                int mm = __ldg(p.row_info + g);
+                mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
+                run += (mm + 2 * kBM - 1) / (2 * kBM) * p.num_n_tiles;
+            }
+            if (lane == 31) list[G] = incl;
+        }
+        __syncthreads();
+        total_units = list[p.num_groups];
+    }
+    return total_units;
+}
+
+// Unit u -> (group, column tile, this CTA's 128-row half).  Contiguous units are
+// rasterised in bands of 4 pair-list entries times all column tiles, column
+// tile slowest within a band, so the B tiles of a band are reused from L2.
+template <bool kMasked>
+__device__ __forceinline__ PairUnit unit_of(const GemmParams& p, const int* list, int total_units,
+                                            int u, uint32_t rank) {
+    PairUnit w;
+    if constexpr (!kMasked) {
+        const int P = total_units / p.num_n_tiles;
+        const int band_units = 4 * p.num_n_tiles;
+        const int band = u / band_units;
+        const int r = u - band * band_units;
+        const int gp = min(4, P - band * 4);
+        const int pi = band * 4 + r % gp;
+        w.n_tile = r / gp;
+        const uint32_t e = static_cast<uint32_t>(list[pi]);
+        const int t0 = static_cast<int>(e & 0xFFFu);
+        const bool half = (e >> 12) & 1u;
+        w.g = static_cast<int>(e >> 13);
+        w.m_base = (t0 + static_cast<int>(rank)) * kBM;
+        w.store = !(half && rank == 1);
+    } else {
+        int lo = 0, hi = p.num_groups;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (list[mid] <= u) lo = mid; else hi = mid;
+        }
+        const int local = u - list[lo];
+        const int mp = (list[lo + 1] - list[lo]) / p.num_n_tiles;
+        w.g = lo;
+        w.n_tile = local / mp;
+        w.m_base = (local - w.n_tile * mp) * 2 * kBM + static_cast<int>(rank) * kBM;
+        w.store = true;
+    }
+    return w;
+}
 
 template <typename OutT, bool kMasked, bool kSwiglu>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -300,126 +439,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tmem_relinquish_pair();
     }
 
-    int total_units;
-    if constexpr (!kMasked) {
-        // ---- pair list: tiles of each expert segment, two by two
-        const int T = p.num_m_tiles;
-        int* E = reinterpret_cast<int*>(smem + L::kOffA);  // scratch (stage buffers are idle)
-        // all of this thread's grouped_layout reads are issued before the first is used
-        constexpr int kLoads = kPairMaxTiles / kThreads;
-        int ev[kLoads];
-#pragma unroll
-        for (int j = 0; j < kLoads; ++j) {
-            const int t = static_cast<int>(threadIdx.x) + j * kThreads;
-            ev[j] = t < T ? __ldg(p.row_info + static_cast<int64_t>(t) * kBM) : -1;
-        }
-#pragma unroll
-        for (int j = 0; j < kLoads; ++j) {
-            const int t = static_cast<int>(threadIdx.x) + j * kThreads;
-            if (t < T) {
-                int v = ev[j];
-                if (v >= p.num_groups || v < -1) {
-                    raise_error(p.err, kErrBadGroup);
-                    v = -1;
-                }
-                E[t] = v;
-            }
-        }
-        __syncthreads();
-        const int chunk = (T + kThreads - 1) / kThreads;
-        const int lo = min(T, static_cast<int>(threadIdx.x) * chunk);
-        const int hi = min(T, lo + chunk);
-        int last_start = -1;
-        for (int t = lo; t < hi; ++t)
-            if (t == 0 || E[t] != E[t - 1]) last_start = t;
-        const int carry = block_exclusive_max(last_start, scan_scratch);
-        int start = carry, count = 0;
-        for (int t = lo; t < hi; ++t) {
-            if (t == 0 || E[t] != E[t - 1]) start = t;
-            if (E[t] >= 0 && ((t - start) & 1) == 0) ++count;
-        }
-        int total = 0;
-        int idx = block_exclusive_sum(count, scan_scratch, &total);
-        start = carry;
-        for (int t = lo; t < hi; ++t) {
-            if (t == 0 || E[t] != E[t - 1]) start = t;
-            if (E[t] >= 0 && ((t - start) & 1) == 0) {
-                const bool half = (t + 1 >= T) || (E[t + 1] != E[t]);
-                list[idx++] = static_cast<int>(pack_pair(t, half, E[t]));
-            }
-        }
-        total_units = total * p.num_n_tiles;
-    } else {
-        // ---- masked: pairs per group and their prefix (warp 3)
-        if (warp == 3) {
-            const int G = p.num_groups;
-            const int per = (G + 31) / 32;
-            const int g0 = lane * per;
-            int local = 0;
-            for (int g = g0; g < min(G, g0 + per); ++g) {
-                int mm = __ldg(p.row_info + g);
-                if (mm < 0 || mm > p.rows) {
-                    raise_error(p.err, kErrMaskedM);
-                    mm = mm < 0 ? 0 : static_cast<int>(p.rows);
-                }
-                local += (mm + 2 * kBM - 1) / (2 * kBM) * p.num_n_tiles;
-            }
-            int incl = local;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += v;
-            }
-            int run = incl - local;
-            for (int g = g0; g < min(G, g0 + per); ++g) {
-                list[g] = run;
-                int mm = __ldg(p.row_info + g);
-                mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
-                run += (mm + 2 * kBM - 1) / (2 * kBM) * p.num_n_tiles;
-            }
-            if (lane == 31) list[G] = incl;
-        }
-        __syncthreads();
-        total_units = list[p.num_groups];
-    }
+    const int total_units = build_units<kMasked, kThreads>(p, smem + L::kOffA, list, scan_scratch);
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // peer barriers initialised, tensor memory allocated in both CTAs
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // unit u -> (group, n tile, this CTA's 128-row half)
-    auto get_unit = [&](int u) -> PairUnit {
-        PairUnit w;
-        if constexpr (!kMasked) {
-            const int P = total_units / p.num_n_tiles;
-            const int band_units = 4 * p.num_n_tiles;
-            const int band = u / band_units;
-            const int r = u - band * band_units;
-            const int gp = min(4, P - band * 4);
-            const int pi = band * 4 + r % gp;
-            w.n_tile = r / gp;
-            const uint32_t e = static_cast<uint32_t>(list[pi]);
-            const int t0 = static_cast<int>(e & 0xFFFu);
-            const bool half = (e >> 12) & 1u;
-            w.g = static_cast<int>(e >> 13);
-            w.m_base = (t0 + static_cast<int>(rank)) * kBM;
-            w.store = !(half && rank == 1);
-        } else {
-            int lo = 0, hi = p.num_groups;
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (list[mid] <= u) lo = mid; else hi = mid;
-            }
-            const int local = u - list[lo];
-            const int mp = (list[lo + 1] - list[lo]) / p.num_n_tiles;
-            w.g = lo;
-            w.n_tile = local / mp;
-            w.m_base = (local - w.n_tile * mp) * 2 * kBM + static_cast<int>(rank) * kBM;
-            w.store = true;
-        }
-        return w;
-    };
+    auto get_unit = [&](int u) { return unit_of<kMasked>(p, list, total_units, u, rank); };
 
     constexpr uint32_t kIdesc = make_idesc_mxf8(2 * kBM, 256);
     const int KB = p.kb_count;

@@ -186,6 +186,36 @@ int gemm_grouped_masked_silu_mul_quant(const void* a, const float* scale_a, int 
                                        int64_t n, int64_t k, void* stream);
 
 /*
+ * Grouped GEMM with arbitrary fp32 block scales (software promotion).
+ *
+ * Same arguments, layouts and results contract as gemm_grouped_contiguous /
+ * gemm_grouped_masked, but scale_a and scale_b may hold any finite fp32
+ * values, not only the powers of two the tensor core applies itself: the
+ * product of each 128-K block is formed without scales (tcgen05.mma
+ * kind::f8f6f4), then multiplied by sa[r, kb] * sb[g, n/128, kb] (rounded to
+ * fp32) and added in fp32 by the CUDA cores -- the promotion scheme of the
+ * DeepGEMM path the "Adds Grouped and Batched GEMM kernels with blockscaling
+ * matching DeepGEMM API" page (DeepGEMM conformance details) describes for
+ * hardware without scaled matrix instructions.  Also an independent check of
+ * the hardware-scaled path on power-of-two scales.
+ *
+ * Runs on the CTA-pair kernel only: n % 256 == 0, d 32-byte aligned, and for
+ * the contiguous variant m_sum <= 524288 rows and num_groups < 2^18; other
+ * shapes return FP8BS_ERR_INVALID_ARG.  No scratch memory, no stream-K tail.
+ */
+int gemm_grouped_contiguous_fp32_scales(const void* a, const float* scale_a, int sa_layout,
+                                        int64_t ld_sa, const void* b, const float* scale_b,
+                                        const int32_t* grouped_layout, void* d, int out_dtype,
+                                        int64_t m_sum, int64_t n, int64_t k, int64_t num_groups,
+                                        void* stream);
+
+int gemm_grouped_masked_fp32_scales(const void* a, const float* scale_a, int sa_layout,
+                                    int64_t ld_sa, const void* b, const float* scale_b,
+                                    const int32_t* masked_m, int64_t expected_m, void* d,
+                                    int out_dtype, int64_t num_groups, int64_t m_max, int64_t n,
+                                    int64_t k, void* stream);
+
+/*
  * Contiguous grouped GEMM that allocates no device memory.  (No counterpart on
  * the pages: an addition for callers that may not call cudaMalloc -- for
  * example code that runs under a memory pool or allocator that owns all device

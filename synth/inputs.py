@@ -63,6 +63,11 @@ CONFIGS: Dict[str, dict] = {
     "c7_swiglu_contig_g8_m1024_n4096_k7168": dict(
         variant="contiguous", G=8, N=4096, K=7168, out=OUT_BF16, sa_layout=SA_KM,
         sizes=("fixed", 1024), seed=7, epilogue="silu_mul_quant"),
+    # workload 2's shape with arbitrary fp32 block scales (amax / 448, not rounded to a
+    # power of two), run by the software-promotion kernel
+    "c8_fp32scales_contig_g8_m1024_n2048_k7168": dict(
+        variant="contiguous", G=8, N=2048, K=7168, out=OUT_BF16, sa_layout=SA_KM,
+        sizes=("fixed", 1024), seed=8, scale_kind="fp32"),
 }
 
 
@@ -81,26 +86,34 @@ def ceil_to_ue8m0_f32(t: torch.Tensor) -> torch.Tensor:
     return (expo << 23).view(torch.float32)
 
 
-def quantize_a_blocks(x: torch.Tensor):
-    """(1,128) blocks of a [R, K] fp32 matrix -> (e4m3 codes uint8 [R,K], fp32 scales [R,K/128])."""
+def _block_scale(amax: torch.Tensor, pow2: bool) -> torch.Tensor:
+    """amax / 448, rounded up to a power of two (UE8M0) unless pow2 is False."""
+    t = amax / E4M3_MAX
+    return ceil_to_ue8m0_f32(t) if pow2 else t
+
+
+def quantize_a_blocks(x: torch.Tensor, pow2: bool = True):
+    """(1,128) blocks of a [R, K] fp32 matrix -> (e4m3 codes uint8 [R,K], fp32 scales [R,K/128]).
+
+    pow2=False keeps the plain fp32 scale amax / 448 (arbitrary fp32 scales)."""
     r, k = x.shape
     if k % 128:
         raise ValueError("K must be a multiple of 128")
     xb = x.float().reshape(r, k // 128, 128)
     amax = xb.abs().amax(dim=2).clamp(min=AMAX_FLOOR)
-    s = ceil_to_ue8m0_f32(amax / E4M3_MAX)
+    s = _block_scale(amax, pow2)
     q = (xb / s.unsqueeze(2)).to(torch.float8_e4m3fn).view(torch.uint8).reshape(r, k)
     return q, s
 
 
-def quantize_b_blocks(x: torch.Tensor):
+def quantize_b_blocks(x: torch.Tensor, pow2: bool = True):
     """(128,128) blocks of an [N, K] fp32 matrix -> (codes uint8 [N,K], scales [N/128,K/128])."""
     n, k = x.shape
     if k % 128 or n % 128:
         raise ValueError("N and K must be multiples of 128")
     xb = x.float().reshape(n // 128, 128, k // 128, 128)
     amax = xb.abs().amax(dim=(1, 3)).clamp(min=AMAX_FLOOR)
-    s = ceil_to_ue8m0_f32(amax / E4M3_MAX)
+    s = _block_scale(amax, pow2)
     q = (xb / s[:, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(n, k)
     return q, s
 
@@ -159,6 +172,7 @@ class Problem:
     row_offsets: Optional[List[int]] = None        # contiguous: first row of each group
     pad_multiple: int = 128
     epilogue: str = ""    # "" (bf16/f16 D) or "silu_mul_quant" (E4M3 codes + scales of SiLU(gate)*up)
+    scale_kind: str = "ue8m0"  # "ue8m0" (power-of-two scales) or "fp32" (amax / 448 as is)
 
     @property
     def KB(self) -> int:
@@ -236,15 +250,20 @@ class Problem:
 
 def make_problem(variant: str, G: int, N: int, K: int, group_sizes, *, out_dtype=OUT_BF16,
                  sa_layout=SA_MK, seed: int = 0, M_max: int = 0, pad_multiple: int = 128,
-                 device="cpu", name: str = "custom", tail_rows: int = 0) -> Problem:
+                 device="cpu", name: str = "custom", tail_rows: int = 0,
+                 scale_kind: str = "ue8m0") -> Problem:
     """Build a problem from explicit group sizes.
 
     contiguous: group g owns round_up(group_sizes[g], pad_multiple) rows, the
     trailing ones marked -1; ``tail_rows`` extra -1 rows are appended at the
     end (a ragged M_sum).  masked: A is [G, M_max, K] and masked_m = group_sizes.
     Padding and masked rows hold random data too, so a kernel that wrongly
-    computes or stores them is caught.
+    computes or stores them is caught.  scale_kind "fp32" keeps each block's
+    scale at amax / 448 instead of rounding it up to a power of two.
     """
+    if scale_kind not in ("ue8m0", "fp32"):
+        raise ValueError(f"unknown scale_kind {scale_kind!r}")
+    pow2 = scale_kind == "ue8m0"
     sizes = [int(s) for s in group_sizes]
     if len(sizes) != G:
         raise ValueError("one size per group")
@@ -252,7 +271,7 @@ def make_problem(variant: str, G: int, N: int, K: int, group_sizes, *, out_dtype
     b_codes = torch.empty((G, N, K), dtype=torch.uint8, device=device)
     sb = torch.empty((G, N // 128, KB), dtype=torch.float32, device=device)
     for g in range(G):
-        q, s = quantize_b_blocks(_randn((N, K), _sub_seed(seed, 2, g), device))
+        q, s = quantize_b_blocks(_randn((N, K), _sub_seed(seed, 2, g), device), pow2)
         b_codes[g] = q
         sb[g] = s
     if variant == "contiguous":
@@ -266,12 +285,12 @@ def make_problem(variant: str, G: int, N: int, K: int, group_sizes, *, out_dtype
         for g in range(G):
             lo, hi = offsets[g], offsets[g + 1]
             if hi > lo:
-                q, s = quantize_a_blocks(_randn((hi - lo, K), _sub_seed(seed, 1, g), device))
+                q, s = quantize_a_blocks(_randn((hi - lo, K), _sub_seed(seed, 1, g), device), pow2)
                 a_codes[lo:hi] = q
                 sa_mk[lo:hi] = s
                 layout[lo:lo + sizes[g]] = g
         if tail_rows:
-            q, s = quantize_a_blocks(_randn((tail_rows, K), _sub_seed(seed, 3, 0), device))
+            q, s = quantize_a_blocks(_randn((tail_rows, K), _sub_seed(seed, 3, 0), device), pow2)
             a_codes[offsets[-1]:] = q
             sa_mk[offsets[-1]:] = s
         if sa_layout == SA_KM:
@@ -283,14 +302,14 @@ def make_problem(variant: str, G: int, N: int, K: int, group_sizes, *, out_dtype
         return Problem(name=name, variant=variant, G=G, N=N, K=K, out_dtype=out_dtype,
                        sa_layout=sa_layout, seed=seed, group_sizes=sizes, a=a_codes, sa=sa,
                        ld_sa=ld, b=b_codes, sb=sb, grouped_layout=layout, row_offsets=offsets,
-                       pad_multiple=pad_multiple)
+                       pad_multiple=pad_multiple, scale_kind=scale_kind)
     if variant == "masked":
         if M_max <= 0 or max(sizes) > M_max:
             raise ValueError("masked: need 0 < max(masked_m) <= M_max")
         a_codes = torch.empty((G, M_max, K), dtype=torch.uint8, device=device)
         sa_mk = torch.empty((G, M_max, KB), dtype=torch.float32, device=device)
         for g in range(G):
-            q, s = quantize_a_blocks(_randn((M_max, K), _sub_seed(seed, 1, g), device))
+            q, s = quantize_a_blocks(_randn((M_max, K), _sub_seed(seed, 1, g), device), pow2)
             a_codes[g] = q
             sa_mk[g] = s
         if sa_layout == SA_KM:
@@ -302,7 +321,7 @@ def make_problem(variant: str, G: int, N: int, K: int, group_sizes, *, out_dtype
         mm = torch.tensor(sizes, dtype=torch.int32, device=device)
         return Problem(name=name, variant=variant, G=G, N=N, K=K, out_dtype=out_dtype,
                        sa_layout=sa_layout, seed=seed, group_sizes=sizes, a=a_codes, sa=sa,
-                       ld_sa=ld, b=b_codes, sb=sb, masked_m=mm, M_max=M_max)
+                       ld_sa=ld, b=b_codes, sb=sb, masked_m=mm, M_max=M_max, scale_kind=scale_kind)
     raise ValueError(f"unknown variant {variant!r}")
 
 
@@ -312,7 +331,7 @@ def make_config(name: str, device="cpu") -> Problem:
     sizes = draw_group_sizes(c["sizes"], c["G"], c["seed"])
     p = make_problem(c["variant"], c["G"], c["N"], c["K"], sizes, out_dtype=c["out"],
                      sa_layout=c["sa_layout"], seed=c["seed"], M_max=c.get("M_max", 0),
-                     device=device, name=name)
+                     device=device, name=name, scale_kind=c.get("scale_kind", "ue8m0"))
     p.epilogue = c.get("epilogue", "")
     return p
 

@@ -41,10 +41,13 @@ def run_gpu(p, d=None, stream=None):
         d = torch.full(shape, SENTINEL, dtype=torch.int16 if SENTINEL < 0x8000 else torch.int32,
                        device=p.a.device).view(out_torch_dtype(p))
     sa = p.sa_mk_view()
+    promote = p.scale_kind == "fp32"   # arbitrary fp32 scales: the software-promotion kernel
     if p.variant == "contiguous":
-        fb.gemm_grouped_contiguous(p.a, sa, p.b, p.sb, d, p.grouped_layout, stream=stream)
+        fn = fb.gemm_grouped_contiguous_fp32_scales if promote else fb.gemm_grouped_contiguous
+        fn(p.a, sa, p.b, p.sb, d, p.grouped_layout, stream=stream)
     else:
-        fb.gemm_grouped_masked(p.a, sa, p.b, p.sb, d, p.masked_m, stream=stream)
+        fn = fb.gemm_grouped_masked_fp32_scales if promote else fb.gemm_grouped_masked
+        fn(p.a, sa, p.b, p.sb, d, p.masked_m, stream=stream)
     torch.cuda.synchronize()
     err = fb.device_error()
     assert err == 0, f"device error word {err:#x}"

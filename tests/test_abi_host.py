@@ -190,3 +190,37 @@ def test_fused_empty_is_noop(lib):
     assert _fused(m_sum=0, a=0, out=0, os=0) == OK
     assert _fused_masked(m_max=0, a=0, out=0, os=0) == OK
     assert _fused(m_sum=0, n=384) == INVALID
+
+
+def _fp32s(**kw):
+    args = dict(a=P, sa=P, sa_layout=0, ld_sa=0, b=P, sb=P, lay=P, d=P, out=0,
+                m_sum=256, n=256, k=256, g=2)
+    args.update(kw)
+    return _binding.gemm_grouped_contiguous_fp32_scales_raw(
+        args["a"], args["sa"], args["sa_layout"], args["ld_sa"], args["b"], args["sb"],
+        args["lay"], args["d"], args["out"], args["m_sum"], args["n"], args["k"], args["g"], 0)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(n=384),                 # the promotion kernel is a CTA-pair kernel: n % 256 == 0
+    dict(d=P + 16),              # 32-byte output stores
+    dict(m_sum=524288 + 128), dict(g=1 << 18),
+    dict(a=0), dict(sa=0), dict(lay=0), dict(k=100), dict(out=2), dict(sa_layout=1, ld_sa=255),
+])
+def test_fp32_scales_rejects(lib, bad):
+    assert _fp32s(**bad) == INVALID
+
+
+def test_fp32_scales_masked_rejects_and_empty(lib):
+    def call(**kw):
+        args = dict(a=P, sa=P, sa_layout=0, ld_sa=0, b=P, sb=P, mm=P, d=P, out=0, g=2, m_max=64,
+                    n=256, k=256)
+        args.update(kw)
+        return _binding.gemm_grouped_masked_fp32_scales_raw(
+            args["a"], args["sa"], args["sa_layout"], args["ld_sa"], args["b"], args["sb"],
+            args["mm"], 0, args["d"], args["out"], args["g"], args["m_max"], args["n"],
+            args["k"], 0)
+    for bad in (dict(n=384), dict(d=P + 16), dict(mm=0), dict(g=0), dict(m_max=-1)):
+        assert call(**bad) == INVALID, bad
+    assert call(m_max=0, a=0) == OK
+    assert _fp32s(m_sum=0, a=0, d=0) == OK

@@ -208,6 +208,28 @@ def test_contiguous_matches_exact_rationals(oracle_mod, sa_layout):
         assert all(float(acc[i, j]) == float(brute[r][j]) for j in range(acc.shape[1]))
 
 
+def test_contiguous_with_arbitrary_fp32_scales_vs_exact_rationals(oracle_mod):
+    """Scales that are not powers of two (the inputs of the software-promotion
+    path): the oracle's fp64 result is within a few fp64 ulps of the exact
+    rational value (no exactness argument holds any more, but nothing coarser
+    than fp64 rounding may appear)."""
+    rng = np.random.default_rng(21)
+    a, sa, b, sb, layout = _random_small_problem(rng, 2, [3, 2], 256, 384, exp_range=(-9, -4))
+    sa = (sa * rng.uniform(1.0, 2.0, sa.shape)).astype(np.float32)
+    sb = (sb * rng.uniform(1.0, 2.0, sb.shape)).astype(np.float32)
+    assert np.any(np.frexp(sa)[0] != 0.5) and np.any(np.frexp(sb)[0] != 0.5)
+    acc, valid, rows = oracle.grouped_contiguous(a, sa, SA_MK, b, sb, layout)
+    brute = _brute_contiguous(a, sa, SA_MK, b, sb, layout)
+    # the same sums over |terms| (sign bits cleared) bound the rounding of the fp64 ones
+    mags = _brute_contiguous(a & 0x7F, sa, SA_MK, b & 0x7F, sb, layout)
+    for i, r in enumerate(rows):
+        if not valid[i]:
+            continue
+        for j in range(acc.shape[1]):
+            err = abs(Fraction(float(acc[i, j])) - brute[r][j])
+            assert err <= mags[r][j] * Fraction(1, 2 ** 48)
+
+
 def test_contiguous_exact_with_realistic_scale_spread(oracle_mod):
     """Scales within 2^-9..2^-5 (the spread ceil_to_ue8m0 gives N(0,1) data) and
     four K-blocks: the fp64 sum is the exact rational value, bit for bit."""

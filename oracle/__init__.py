@@ -27,6 +27,9 @@ Parity status of every function (see tests/test_oracle_pins.py):
                     pre-quantisation fp32 product within calc_diff 1e-3
   calc_diff         pinned: closed forms
   block_dot_exact   pinned: exact-rational brute force
+  e2m1 / e8m0       pinned: the 16 E2M1 values derived by hand; E8M0 closed form
+  mxfp4 GEMM        pinned: exact-rational brute force, integer matmul, power-of-two
+                    scale exactness, masked == contiguous, nibble order
   silu_mul_quant    pinned: hand-derived golden blocks, SiLU closed forms and the
                     identity silu(x) - silu(-x) = x, quantiser invariants (power-of-two
                     scale, |h|/s <= 448, half-spacing error, sign), zero blocks
@@ -86,6 +89,16 @@ def _load():
     lib.fp8bs_oracle_block_dot_exact.restype = ctypes.c_double
     lib.fp8bs_oracle_silu_mul_quant.argtypes = [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P, _P]
     lib.fp8bs_oracle_silu_mul_quant.restype = ctypes.c_int
+    lib.fp8bs_oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+    lib.fp8bs_oracle_e2m1_to_double.restype = ctypes.c_double
+    lib.fp8bs_oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+    lib.fp8bs_oracle_e8m0_to_double.restype = ctypes.c_double
+    lib.fp8bs_oracle_mxfp4_contiguous.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                                  _P, _I64, _P, _P]
+    lib.fp8bs_oracle_mxfp4_contiguous.restype = ctypes.c_int
+    lib.fp8bs_oracle_mxfp4_masked.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                              _P, _I64, _P, _P]
+    lib.fp8bs_oracle_mxfp4_masked.restype = ctypes.c_int
     lib.fp8bs_oracle_max_threads.argtypes = []
     lib.fp8bs_oracle_max_threads.restype = ctypes.c_int
     _lib = lib
@@ -267,3 +280,67 @@ def silu_mul_quant(acc_gate_up):
     if rc != 0:
         raise ValueError("oracle: invalid arguments")
     return {"h": h, "q": q, "s": s, "margin": margin, "tmargin": tmargin}
+
+
+# ----------------------------------------------------------------- MXFP4 grouped GEMM
+def e2m1_decode(codes) -> np.ndarray:
+    """E2M1 4-bit codes (0..15) -> fp64 values, from the format definition."""
+    lib = _load()
+    codes = np.asarray(codes, dtype=np.uint8)
+    flat = [lib.fp8bs_oracle_e2m1_to_double(int(c) & 0xF) for c in codes.reshape(-1)]
+    return np.array(flat, dtype=np.float64).reshape(codes.shape)
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    """E8M0 scale bytes -> 2^(e - 127) (NaN for 255)."""
+    lib = _load()
+    codes = np.asarray(codes, dtype=np.uint8)
+    flat = [lib.fp8bs_oracle_e8m0_to_double(int(c)) for c in codes.reshape(-1)]
+    return np.array(flat, dtype=np.float64).reshape(codes.shape)
+
+
+def mxfp4_contiguous(a_packed, scale_a, b_packed, scale_b, grouped_layout, rows=None):
+    """Contiguous MXFP4 grouped GEMM for the listed rows (default: all).
+
+    a_packed uint8 [M_sum, K/2] (element 2i in the low nibble of byte i)
+    scale_a  uint8 [M_sum, K/32] E8M0;  b_packed uint8 [G, N, K/2];
+    scale_b  uint8 [G, N, K/32];  grouped_layout int32 [M_sum], -1 = padding.
+    Returns (acc fp64 [len(rows), N], valid bool, rows).
+    """
+    a = _c(a_packed, np.uint8)
+    b = _c(b_packed, np.uint8)
+    sa = _c(scale_a, np.uint8)
+    sb = _c(scale_b, np.uint8)
+    lay = _c(grouped_layout, np.int32)
+    m_sum, kh = a.shape
+    g_count, n, _ = b.shape
+    rows = np.arange(m_sum, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    acc = np.empty((rows.size, n), dtype=np.float64)
+    valid = np.empty(rows.size, dtype=np.uint8)
+    rc = _load().fp8bs_oracle_mxfp4_contiguous(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(lay),
+                                               m_sum, n, 2 * kh, g_count, _ptr(rows), rows.size,
+                                               _ptr(acc), _ptr(valid))
+    if rc != 0:
+        raise ValueError("oracle: invalid arguments")
+    return acc, valid.astype(bool), rows
+
+
+def mxfp4_masked(a_packed, scale_a, b_packed, scale_b, masked_m, rows=None):
+    """Masked MXFP4 grouped GEMM: a_packed [G, M_max, K/2], scale_a [G, M_max, K/32]."""
+    a = _c(a_packed, np.uint8)
+    b = _c(b_packed, np.uint8)
+    sa = _c(scale_a, np.uint8)
+    sb = _c(scale_b, np.uint8)
+    mm = _c(masked_m, np.int32)
+    g_count, m_max, kh = a.shape
+    _, n, _ = b.shape
+    rows = (np.arange(g_count * m_max, dtype=np.int64) if rows is None
+            else _c(rows, np.int64))
+    acc = np.empty((rows.size, n), dtype=np.float64)
+    valid = np.empty(rows.size, dtype=np.uint8)
+    rc = _load().fp8bs_oracle_mxfp4_masked(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(mm),
+                                           g_count, m_max, n, 2 * kh, _ptr(rows), rows.size,
+                                           _ptr(acc), _ptr(valid))
+    if rc != 0:
+        raise ValueError("oracle: invalid arguments")
+    return acc, valid.astype(bool), rows

@@ -390,3 +390,116 @@ int fp8bs_oracle_silu_mul_quant(const double* gate, const double* up, int64_t ro
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * MXFP4 (a4w4) grouped GEMM.
+ *
+ * [P3] "flydsl mxfp4 a4w4 MoE: bring gemm1/gemm2 to parity with the HIP
+ *      backend", Summary: the MoE GEMMs with both operands in MXFP4.
+ * [OMX] the OCP Microscaling (MX) formats: E2M1 elements -- a sign bit, two
+ *      exponent bits with bias 1 and one mantissa bit, magnitudes 0, 0.5, 1,
+ *      1.5, 2, 3, 4, 6, no infinity or NaN -- in blocks of 32 consecutive
+ *      elements along K that share one E8M0 scale 2^(e - 127) (e = 255 is NaN).
+ *
+ * Storage: two elements per byte, element 2i in the low nibble of byte i;
+ * scales one byte each, sa [rows, K/32] (masked: [G, M_max, K/32]) and
+ * sb [G, N, K/32].  For every computed row r of group g and column n:
+ *     acc = sum_j 2^(sa[r,j]-127) * 2^(sb[g,n,j]-127)
+ *                 * sum_{k in block j} e2m1(A[r,k]) * e2m1(B[g,n,k])      (fp64)
+ * Every block sum is a multiple of 1/4 below 32 * 36 and the scales are
+ * powers of two, so acc is exact while the scale exponents span less than
+ * about 40 binades.
+ * ------------------------------------------------------------------------ */
+double fp8bs_oracle_e2m1_to_double(uint8_t code) {
+    int sign = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+double fp8bs_oracle_e8m0_to_double(uint8_t e) {
+    if (e == 0xFF) return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+static double e2m1_at(const uint8_t* packed, int64_t row_bytes, int64_t row, int64_t k) {
+    const uint8_t byte = packed[row * row_bytes + k / 2];
+    return fp8bs_oracle_e2m1_to_double((uint8_t)((k & 1) ? (byte >> 4) : (byte & 0xF)));
+}
+
+static void mx_row(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                   int64_t arow, int64_t g, int64_t n_dim, int64_t k_dim, double* acc) {
+    const int64_t nblk = k_dim / 32;
+    int64_t n, j, k;
+    for (n = 0; n < n_dim; ++n) {
+        const int64_t brow = g * n_dim + n;
+        double total = 0.0;
+        for (j = 0; j < nblk; ++j) {
+            double dot = 0.0;
+            for (k = j * 32; k < j * 32 + 32; ++k)
+                dot += e2m1_at(a, k_dim / 2, arow, k) * e2m1_at(b, k_dim / 2, brow, k);
+            total += fp8bs_oracle_e8m0_to_double(sa[arow * nblk + j]) *
+                     fp8bs_oracle_e8m0_to_double(sb[brow * nblk + j]) * dot;
+        }
+        acc[n] = total;
+    }
+}
+
+int fp8bs_oracle_mxfp4_contiguous(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
+                                  const uint8_t* sb, const int32_t* grouped_layout,
+                                  int64_t m_sum, int64_t n_dim, int64_t k_dim,
+                                  int64_t num_groups, const int64_t* rows, int64_t nrows,
+                                  double* acc, uint8_t* valid) {
+    int64_t i;
+    int bad = 0;
+    if (k_dim % 32 || n_dim <= 0) return -1;
+    for (i = 0; i < nrows; ++i) {
+        int64_t r = rows[i];
+        if (r < 0 || r >= m_sum) bad = 1;
+        else if (grouped_layout[r] >= num_groups || grouped_layout[r] < -1) bad = 1;
+    }
+    if (bad) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = 0; i < nrows; ++i) {
+        int64_t r = rows[i];
+        int64_t g = grouped_layout[r];
+        int64_t n;
+        if (g < 0) {
+            valid[i] = 0;
+            for (n = 0; n < n_dim; ++n) acc[i * n_dim + n] = NAN;
+            continue;
+        }
+        valid[i] = 1;
+        mx_row(a, sa, b, sb, r, g, n_dim, k_dim, acc + i * n_dim);
+    }
+    return 0;
+}
+
+int fp8bs_oracle_mxfp4_masked(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
+                              const uint8_t* sb, const int32_t* masked_m, int64_t num_groups,
+                              int64_t m_max, int64_t n_dim, int64_t k_dim, const int64_t* rows,
+                              int64_t nrows, double* acc, uint8_t* valid) {
+    int64_t i;
+    int bad = 0;
+    if (k_dim % 32 || n_dim <= 0) return -1;
+    for (i = 0; i < nrows; ++i)
+        if (rows[i] < 0 || rows[i] >= num_groups * m_max) bad = 1;
+    for (i = 0; i < num_groups; ++i)
+        if (masked_m[i] < 0 || masked_m[i] > m_max) bad = 1;
+    if (bad) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (i = 0; i < nrows; ++i) {
+        int64_t f = rows[i];
+        int64_t g = f / m_max, m = f % m_max;
+        int64_t n;
+        if (m >= masked_m[g]) {
+            valid[i] = 0;
+            for (n = 0; n < n_dim; ++n) acc[i * n_dim + n] = NAN;
+            continue;
+        }
+        valid[i] = 1;
+        mx_row(a, sa, b, sb, f, g, n_dim, k_dim, acc + i * n_dim);
+    }
+    return 0;
+}

@@ -37,7 +37,8 @@ import torch  # noqa: E402
 
 DEFAULT_WORKLOAD = "c2_contig_g8_m1024_n2048_k7168"
 METRIC = "grouped FP8 GEMM TFLOP/s (2*sum(m)*N*K/t)"
-FP8_OVER_BF16 = 4.5 / 2.25  # nominal dense tensor-core ratio of GB300
+FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense tensor-core ratios of GB300
+FP4_OVER_BF16 = 13.5 / 2.25
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 CSRC = os.path.join(ROOT, "fp8_block_scaled_gb300", "csrc")
@@ -189,7 +190,12 @@ def out_dtype_of(p):
 
 
 def run_once(fb, p, a, sa, b, sb, rowinfo, d, stream=None):
-    if p.epilogue == "silu_mul_quant":
+    if p.is_mx:
+        if p.variant == "contiguous":
+            fb.gemm_grouped_contiguous_mxfp4(a, sa, b, sb, d, rowinfo, stream=stream)
+        else:
+            fb.gemm_grouped_masked_mxfp4(a, sa, b, sb, d, rowinfo, stream=stream)
+    elif p.epilogue == "silu_mul_quant":
         q, qs = d
         if p.variant == "contiguous":
             fb.gemm_grouped_contiguous_silu_mul_quant(a, sa, b, sb, q, qs, rowinfo, stream=stream)
@@ -236,8 +242,10 @@ def describe(p, l2_note):
     cfg = {"workload": p.name, "variant": p.variant, "G": p.G, "N": p.N, "K": p.K,
            "valid_rows": p.valid_rows, "rows": p.rows,
            "out": "bf16" if p.out_dtype == 0 else "f16",
-           "scale_a": "transposed [K/128, M]" if p.sa_layout == 1 else "[M, K/128]",
-           "scales": ("UE8M0 (1,128) activation x (128,128) weight" if p.scale_kind == "ue8m0"
+           "scale_a": ("E8M0 [M, K/32]" if p.is_mx else
+                       "transposed [K/128, M]" if p.sa_layout == 1 else "[M, K/128]"),
+           "scales": ("E8M0 per 32 elements of A and B rows (MXFP4)" if p.is_mx else
+                      "UE8M0 (1,128) activation x (128,128) weight" if p.scale_kind == "ue8m0"
                       else "arbitrary fp32 (1,128) activation x (128,128) weight, promoted in "
                            "software"),
            "parallelism": "replicas (no exchange step)", "l2": l2_note}
@@ -320,7 +328,9 @@ def bench_ours(args):
     peaks, peaks_kind = load_peaks()
     mean_launch_ms = elapsed_ms / args.steps
     achieved = flops / (mean_launch_ms * 1e-3) / 1e12
-    peak_fp8 = peaks["bf16_tflops"] * FP8_OVER_BF16
+    # the contraction's own dtype: E4M3 (or E2M1 for the MXFP4 workloads)
+    ratio, ratio_name = ((FP4_OVER_BF16, "fp4/bf16") if p.is_mx else (FP8_OVER_BF16, "fp8/bf16"))
+    peak_fp8 = peaks["bf16_tflops"] * ratio
     alg_bytes = p.algorithmic_bytes(out_bytes=2)
     hbm_time = alg_bytes / (peaks["hbm_gbs"] * 1e9)
     tensor_time = flops / (peak_fp8 * 1e12)
@@ -335,7 +345,7 @@ def bench_ours(args):
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak_fp8, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / peak_fp8, 4), "traffic": traffic,
                 "peak_source": f"{peaks_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
-                               f"{FP8_OVER_BF16:g} (nominal fp8/bf16 ratio)",
+                               f"{ratio:g} (nominal {ratio_name} ratio)",
                 "algorithmic": {"flops_per_launch": flops, "bytes_per_launch": alg_bytes},
                 "mean_launch_ms": round(mean_launch_ms, 5)}
     else:
@@ -360,8 +370,11 @@ def bench_ours(args):
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
-            "data": "synthetic (seeded N(0,1), UE8M0 ceil-quantised)",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e2m1" if p.is_mx else "e4m3",
+            "data": ("synthetic (seeded N(0,1), MXFP4-quantised)" if p.is_mx else
+                     "synthetic (seeded N(0,1), fp32 block scales)" if p.scale_kind == "fp32" else
+                     "synthetic (seeded N(0,1), UE8M0 ceil-quantised)"),
             "config": describe(p, l2_note), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clk,
             "roofline_time_ms": {"tensor_at_peak": tensor_time * 1e3, "hbm_at_peak": hbm_time * 1e3}}
@@ -411,6 +424,10 @@ def _oracle_call(p, host, rows):
     import oracle
 
     a, sa, b, sb, ri = host
+    if p.is_mx:
+        if p.variant == "contiguous":
+            return oracle.mxfp4_contiguous(a, sa, b, sb, ri, rows=rows)
+        return oracle.mxfp4_masked(a, sa, b, sb, ri, rows=rows)
     if p.variant == "contiguous":
         res = oracle.grouped_contiguous(a, sa, p.sa_layout, b, sb, ri, rows=rows, ld_sa=p.ld_sa)
     else:

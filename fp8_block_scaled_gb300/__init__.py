@@ -13,7 +13,8 @@ kernels of ``libfp8bs.so``; this package only marshals arguments.  The
 ``*_silu_mul_quant`` entry points fuse the first MoE GEMM's SiLU(gate) * up and
 the (1,128) E4M3 requantisation of its output into the same kernel; the
 ``*_fp32_scales`` entry points take arbitrary fp32 block scales (promoted in
-software instead of by the tensor core).
+software instead of by the tensor core); the ``*_mxfp4`` entry points take both
+operands in MXFP4 (E2M1 with E8M0 scales per 32 elements).
 """
 from ._binding import (  # noqa: F401
     DEVERR_BAD_GROUP,
@@ -32,6 +33,8 @@ from ._binding import (  # noqa: F401
     gemm_grouped_contiguous,
     gemm_grouped_contiguous_fp32_scales,
     gemm_grouped_contiguous_fp32_scales_raw,
+    gemm_grouped_contiguous_mxfp4,
+    gemm_grouped_contiguous_mxfp4_raw,
     gemm_grouped_contiguous_noalloc_raw,
     gemm_grouped_contiguous_raw,
     gemm_grouped_contiguous_silu_mul_quant,
@@ -39,6 +42,8 @@ from ._binding import (  # noqa: F401
     gemm_grouped_masked,
     gemm_grouped_masked_fp32_scales,
     gemm_grouped_masked_fp32_scales_raw,
+    gemm_grouped_masked_mxfp4,
+    gemm_grouped_masked_mxfp4_raw,
     gemm_grouped_masked_raw,
     gemm_grouped_masked_silu_mul_quant,
     gemm_grouped_masked_silu_mul_quant_raw,

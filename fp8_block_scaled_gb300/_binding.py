@@ -31,6 +31,7 @@ DEVERR_BAD_GROUP = 0x8
 EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "gemm_grouped_contiguous_noalloc",
            "gemm_grouped_contiguous_silu_mul_quant", "gemm_grouped_masked_silu_mul_quant",
            "gemm_grouped_contiguous_fp32_scales", "gemm_grouped_masked_fp32_scales",
+           "gemm_grouped_contiguous_mxfp4", "gemm_grouped_masked_mxfp4",
            "fp8bs_device_error", "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version")
 
 _lib = None
@@ -80,6 +81,12 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.gemm_grouped_contiguous_fp32_scales.restype = _I
         lib.gemm_grouped_masked_fp32_scales.argtypes = lib.gemm_grouped_masked.argtypes
         lib.gemm_grouped_masked_fp32_scales.restype = _I
+        lib.gemm_grouped_contiguous_mxfp4.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64,
+                                                      _I64, _P]
+        lib.gemm_grouped_contiguous_mxfp4.restype = _I
+        lib.gemm_grouped_masked_mxfp4.argtypes = [_P, _P, _P, _P, _P, _I64, _P, _I, _I64, _I64,
+                                                  _I64, _I64, _P]
+        lib.gemm_grouped_masked_mxfp4.restype = _I
         lib.fp8bs_device_error.argtypes = [_I, ctypes.POINTER(ctypes.c_uint32)]
         lib.fp8bs_device_error.restype = _I
         lib.fp8bs_status_string.argtypes = [_I]
@@ -354,6 +361,74 @@ def gemm_grouped_masked_silu_mul_quant(a, scale_a, b, scale_b, out, out_scale, m
         out.data_ptr(), out_scale.data_ptr(), olayout, old, G, m_max, n, k, stream)
     _check(st, "gemm_grouped_masked_silu_mul_quant")
     return out, out_scale
+
+
+def gemm_grouped_contiguous_mxfp4_raw(a_ptr, sa_ptr, b_ptr, sb_ptr, layout_ptr, d_ptr, out_dtype,
+                                      m_sum, n, k, num_groups, stream=None) -> int:
+    lib = load()
+    return lib.gemm_grouped_contiguous_mxfp4(a_ptr, sa_ptr, b_ptr, sb_ptr, layout_ptr, d_ptr,
+                                             int(out_dtype), int(m_sum), int(n), int(k),
+                                             int(num_groups), ctypes.c_void_p(_stream_handle(stream)))
+
+
+def gemm_grouped_masked_mxfp4_raw(a_ptr, sa_ptr, b_ptr, sb_ptr, masked_m_ptr, expected_m, d_ptr,
+                                  out_dtype, num_groups, m_max, n, k, stream=None) -> int:
+    lib = load()
+    return lib.gemm_grouped_masked_mxfp4(a_ptr, sa_ptr, b_ptr, sb_ptr, masked_m_ptr,
+                                         int(expected_m), d_ptr, int(out_dtype), int(num_groups),
+                                         int(m_max), int(n), int(k),
+                                         ctypes.c_void_p(_stream_handle(stream)))
+
+
+def _u8(t, name):
+    if t.dtype != torch.uint8 or not t.is_contiguous() or not t.is_cuda:
+        raise TypeError(f"{name} must be a contiguous uint8 CUDA tensor")
+    return t.data_ptr()
+
+
+def gemm_grouped_contiguous_mxfp4(a, scale_a, b, scale_b, d, grouped_layout, *, stream=None):
+    """MXFP4 grouped GEMM, contiguous variant (include/fp8bs.h).
+
+    a uint8 [M_sum, K/2] packed E2M1 (element 2i in the low nibble); scale_a uint8
+    [M_sum, K/32] E8M0; b uint8 [G, N, K/2]; scale_b uint8 [G, N, K/32]; d bf16/f16
+    [M_sum, N]; grouped_layout int32 [M_sum], -1 = padding (not written).
+    """
+    m_sum, kh = a.shape
+    G, n, kh2 = b.shape
+    k = 2 * kh
+    if kh2 != kh or scale_a.shape != (m_sum, k // 32) or scale_b.shape != (G, n, k // 32):
+        raise ValueError("shape mismatch")
+    if d.shape != (m_sum, n) or not d.is_contiguous() or grouped_layout.shape != (m_sum,):
+        raise ValueError("d must be contiguous [M_sum, N], grouped_layout [M_sum]")
+    if grouped_layout.dtype != torch.int32:
+        raise ValueError("grouped_layout must be int32")
+    st = gemm_grouped_contiguous_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
+                                           _u8(scale_b, "scale_b"),
+                                           grouped_layout.contiguous().data_ptr(), d.data_ptr(),
+                                           _out_code(d), m_sum, n, k, G, stream)
+    _check(st, "gemm_grouped_contiguous_mxfp4")
+    return d
+
+
+def gemm_grouped_masked_mxfp4(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0, *,
+                              stream=None):
+    """MXFP4 grouped GEMM, masked variant: a [G, M_max, K/2], scale_a [G, M_max, K/32],
+    d [G, M_max, N]; rows m >= masked_m[g] are not written."""
+    G, m_max, kh = a.shape
+    Gb, n, kh2 = b.shape
+    k = 2 * kh
+    if Gb != G or kh2 != kh or scale_a.shape != (G, m_max, k // 32) or scale_b.shape != (G, n, k // 32):
+        raise ValueError("shape mismatch")
+    if d.shape != (G, m_max, n) or not d.is_contiguous() or masked_m.shape != (G,):
+        raise ValueError("d must be contiguous [G, M_max, N], masked_m [G]")
+    if masked_m.dtype != torch.int32:
+        raise ValueError("masked_m must be int32")
+    st = gemm_grouped_masked_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
+                                       _u8(scale_b, "scale_b"), masked_m.contiguous().data_ptr(),
+                                       expected_m, d.data_ptr(), _out_code(d), G, m_max, n, k,
+                                       stream)
+    _check(st, "gemm_grouped_masked_mxfp4")
+    return d
 
 
 def device_error(device: int = None) -> int:

@@ -243,11 +243,11 @@ int launch(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensor
 
 // CTA-pair kernel: cluster of 2, persistent over at most the number of pairs
 // that fit on the device at once.
-template <typename OutT, bool kMasked, bool kSwiglu = false>
+template <typename OutT, bool kMasked, bool kSwiglu = false, bool kMx = false>
 int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensorMap& tb,
                 const GemmParams& p, int64_t units_bound, cudaStream_t stream) {
-    using L = fp8bs::PairLayout;
-    auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, kMasked, kSwiglu>;
+    using L = fp8bs::PairLayoutT<kMx>;
+    auto kern = fp8bs::grouped_gemm_pair_kernel<OutT, kMasked, kSwiglu, kMx>;
     const int smem = L::kBytes + L::kAlignSlack;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -881,6 +881,125 @@ int gemm_grouped_masked_fp32_scales(const void* a, const float* scale_a, int sa_
     return out_dtype == FP8BS_OUT_BF16
                ? launch_promote<__nv_bfloat16, true>(*st, 28, *ta, *tb, p, units, s)
                : launch_promote<__half, true>(*st, 29, *ta, *tb, p, units, s);
+}
+
+// MXFP4 arguments shared by both variants: packed E2M1 operands (16-byte
+// aligned for TMA), E8M0 scale bytes (4-byte aligned: copied a word at a time),
+// 32-byte aligned output, n % 256 == 0, k % 256 == 0 (128 bytes per K block).
+static int validate_mx(const void* a, const uint8_t* sa, const void* b, const uint8_t* sb,
+                       const void* d, int out_dtype, int64_t n, int64_t k, int64_t num_groups) {
+    if (n <= 0 || k <= 0 || n % 256 || k % 256 || num_groups < 1) return FP8BS_ERR_INVALID_ARG;
+    if (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16) return FP8BS_ERR_INVALID_ARG;
+    if (!a || !sa || !b || !sb || !d) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned(a, 16) || !aligned(b, 16) || !aligned(d, 32) || !aligned(sa, 4) || !aligned(sb, 4))
+        return FP8BS_ERR_INVALID_ARG;
+    if (num_groups * n > INT32_MAX || k > INT32_MAX / 2) return FP8BS_ERR_INVALID_ARG;
+    return FP8BS_OK;
+}
+
+int gemm_grouped_contiguous_mxfp4(const void* a, const uint8_t* scale_a, const void* b,
+                                  const uint8_t* scale_b, const int32_t* grouped_layout, void* d,
+                                  int out_dtype, int64_t m_sum, int64_t n, int64_t k,
+                                  int64_t num_groups, void* stream) {
+    if (m_sum < 0 || m_sum > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (m_sum == 0) {
+        if (n <= 0 || k <= 0 || n % 256 || k % 256 || num_groups < 1 ||
+            (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16))
+            return FP8BS_ERR_INVALID_ARG;
+        return FP8BS_OK;
+    }
+    int v = validate_mx(a, scale_a, b, scale_b, d, out_dtype, n, k, num_groups);
+    if (v != FP8BS_OK) return v;
+    const int64_t m_tiles = (m_sum + 127) / 128;
+    if (!grouped_layout || !aligned(grouped_layout, 4) || m_tiles > fp8bs::kMxMaxTiles ||
+        num_groups >= (1 << 18))
+        return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const CUtensorMap *ta = nullptr, *tb = nullptr;
+    constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
+    // packed rows: k/2 bytes, K blocks of 128 bytes
+    if ((rc = get_map3(dev, a, k / 2, m_sum, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
+    if ((rc = get_map3(dev, b, k / 2, num_groups * n, 128, kKbBox, &tb)) != FP8BS_OK) return rc;
+
+    GemmParams p{};
+    p.sa = reinterpret_cast<const float*>(scale_a);  // E8M0 bytes; the MX kernel reads bytes
+    p.sb = reinterpret_cast<const float*>(scale_b);
+    p.row_info = grouped_layout;
+    p.d = d;
+    p.err = st->err;
+    p.rows = m_sum;
+    p.sa_g_stride = 0;
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(k / 256);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>(m_tiles);
+    p.num_n_tiles = static_cast<int>(n / 256);
+    p.raster_band = 8;
+    const int64_t tiles = m_tiles * p.num_n_tiles;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return out_dtype == FP8BS_OUT_BF16
+               ? launch_pair<__nv_bfloat16, false, false, true>(*st, 20, *ta, *tb, p, tiles, s)
+               : launch_pair<__half, false, false, true>(*st, 21, *ta, *tb, p, tiles, s);
+}
+
+int gemm_grouped_masked_mxfp4(const void* a, const uint8_t* scale_a, const void* b,
+                              const uint8_t* scale_b, const int32_t* masked_m, int64_t expected_m,
+                              void* d, int out_dtype, int64_t num_groups, int64_t m_max,
+                              int64_t n, int64_t k, void* stream) {
+    (void)expected_m;  // scheduling hint only; results never depend on it
+    if (m_max < 0 || num_groups < 1 || num_groups > fp8bs::kMaxMaskedGroups)
+        return FP8BS_ERR_INVALID_ARG;
+    if (m_max > 0 && num_groups * m_max > INT32_MAX - 128) return FP8BS_ERR_INVALID_ARG;
+    if (m_max == 0) {
+        if (n <= 0 || k <= 0 || n % 256 || k % 256 ||
+            (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F16))
+            return FP8BS_ERR_INVALID_ARG;
+        return FP8BS_OK;
+    }
+    int v = validate_mx(a, scale_a, b, scale_b, d, out_dtype, n, k, num_groups);
+    if (v != FP8BS_OK) return v;
+    if (!masked_m || !aligned(masked_m, 4)) return FP8BS_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = device_state(&st);
+    if (rc != FP8BS_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const CUtensorMap *ta = nullptr, *tb = nullptr;
+    constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
+    if ((rc = get_map3(dev, a, k / 2, num_groups * m_max, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
+    if ((rc = get_map3(dev, b, k / 2, num_groups * n, 128, kKbBox, &tb)) != FP8BS_OK) return rc;
+
+    GemmParams p{};
+    p.sa = reinterpret_cast<const float*>(scale_a);
+    p.sb = reinterpret_cast<const float*>(scale_b);
+    p.row_info = masked_m;
+    p.d = d;
+    p.err = st->err;
+    p.rows = m_max;
+    p.sa_g_stride = m_max * (k / 32);  // bytes between groups of scale_a
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    p.num_groups = static_cast<int>(num_groups);
+    p.kb_count = static_cast<int>(k / 256);
+    p.nb_count = static_cast<int>(n / 128);
+    p.num_m_tiles = static_cast<int>((m_max + 127) / 128);
+    p.num_n_tiles = static_cast<int>(n / 256);
+    p.raster_band = 1;
+    const int64_t units = num_groups * ((m_max + 255) / 256) * p.num_n_tiles;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return out_dtype == FP8BS_OUT_BF16
+               ? launch_pair<__nv_bfloat16, true, false, true>(*st, 22, *ta, *tb, p, units, s)
+               : launch_pair<__half, true, false, true>(*st, 23, *ta, *tb, p, units, s);
 }
 
 // Contiguous grouped GEMM that allocates nothing: the CTA-pair kernel with its

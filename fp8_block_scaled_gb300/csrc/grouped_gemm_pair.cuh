@@ -69,17 +69,24 @@
 namespace fp8bs {
 
 constexpr int kPairMaxTiles = 4096;  // contiguous: max 128-row tiles (m_sum <= 524288)
+constexpr int kMxMaxTiles = 3968;    // MXFP4 (larger scale staging): m_sum <= 507904
 
-struct PairLayout {
-    static constexpr int kKbPerStage = 2;                // 128-K blocks per pipeline stage
+// Shared-memory plan of the CTA-pair kernel.  kMx selects the MXFP4 variant:
+// a "K block" is then 128 bytes of packed E2M1 (256 elements) and its scales
+// (one E8M0 byte per 32 elements) are staged by cp.async straight into the
+// tcgen05.cp layout, without the fp32 -> UE8M0 conversion of the E4M3 path.
+template <bool kMx>
+struct PairLayoutT {
+    static constexpr int kKbPerStage = 2;                // K blocks per pipeline stage
     static constexpr int kStages = 3;
     static constexpr int kTileBytes = 128 * kBK;         // 128 rows x one K block
     static constexpr int kAStageBytes = kKbPerStage * kTileBytes;
     static constexpr int kBStageBytes = kKbPerStage * kTileBytes;
-    static constexpr int kSfaBytes = 512;                // per K block
-    static constexpr int kSfbBytes = 1024;               // per K block, both 128-column chunks
-    static constexpr int kSaRawBytes = 512;              // per K block
-    static constexpr int kSbRawBytes = 16;               // per K block
+    // per K block: SFA and SFB in tcgen05.cp order (32x128b matrices of 512 bytes)
+    static constexpr int kSfaBytes = kMx ? 1024 : 512;   // MX: two scale words per row
+    static constexpr int kSfbBytes = kMx ? 2048 : 1024;  // both 128-column chunks
+    static constexpr int kSaRawBytes = kMx ? 0 : 512;    // E4M3 path: raw fp32 scales
+    static constexpr int kSbRawBytes = kMx ? 0 : 16;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kAStageBytes;
     static constexpr int kOffSfa = kOffB + kStages * kBStageBytes;
@@ -96,10 +103,11 @@ struct PairLayout {
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;   // slot, abort, scan scratch
     static constexpr int kMiscBytes = 16 + 2 * 16 * 4;
     static constexpr int kOffList = (kOffMisc + kMiscBytes + 15) / 16 * 16;
-    static constexpr int kListEntries = kPairMaxTiles + 1;
+    static constexpr int kMaxTiles = kMx ? kMxMaxTiles : kPairMaxTiles;
+    static constexpr int kListEntries = kMaxTiles + 1;
     static constexpr int kBytes = kOffList + kListEntries * 4;
     static constexpr int kAlignSlack = 1024;
-    static constexpr int kSfColsPerKb = 4 + 8;
+    static constexpr int kSfColsPerKb = kMx ? 8 + 16 : 4 + 8;
     static constexpr int kTmemCols = 512;
     static_assert(256 + kStages * kKbPerStage * kSfColsPerKb <= kTmemCols, "TMEM budget");
     static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
@@ -107,6 +115,7 @@ struct PairLayout {
     static_assert(kPartChunks * kPartChunkBytes <= kStages * (kAStageBytes + kBStageBytes),
                   "stream-K partial staging");
 };
+using PairLayout = PairLayoutT<false>;
 
 // Contiguous pair-list entry: first 128-row tile (12 bits), "second tile not
 // part of the pair" flag (bit 12), expert id (bits 13..31).
@@ -377,11 +386,11 @@ __device__ __forceinline__ PairUnit unit_of(const GemmParams& p, const int* list
     return w;
 }
 
-template <typename OutT, bool kMasked, bool kSwiglu>
+template <typename OutT, bool kMasked, bool kSwiglu, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const GemmParams p) {
-    using L = PairLayout;
+    using L = PairLayoutT<kMx>;
     constexpr int S = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -449,6 +458,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     auto get_unit = [&](int u) { return unit_of<kMasked>(p, list, total_units, u, rank); };
 
     constexpr uint32_t kIdesc = make_idesc_mxf8(2 * kBM, 256);
+    constexpr uint32_t kIdescMx0 = make_idesc_mxf4(2 * kBM, 256, 0);
+    constexpr uint32_t kIdescMx2 = make_idesc_mxf4(2 * kBM, 256, 2);
     const int KB = p.kb_count;
     const int NKS = (KB + L::kKbPerStage - 1) / L::kKbPerStage;  // pipeline steps per unit
     bool aborted = false;
@@ -560,7 +571,46 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     }
                     if (pf) tma_prefetch_3d(map, 0, prow, kp * L::kKbPerStage);
                 }
-                if (is_a) {
+                if (is_a && kMx) {
+                    // MXFP4: E8M0 bytes, [rows, K/32] for A (masked: per group, sa_g_stride
+                    // bytes apart) and [G*N, K/32] for B.  A K block
+                    // has 8 per row = two 4-byte words; word w of row r goes to lane r % 32,
+                    // column r / 32 of 32x128b matrix w (SFB: matrix 2w + n / 128), the
+                    // layout tcgen05.cp moves into tensor memory unchanged.
+                    const uint8_t* sa8 = reinterpret_cast<const uint8_t*>(p.sa);
+                    const uint8_t* sb8 = reinterpret_cast<const uint8_t*>(p.sb);
+                    const int64_t brow0 =
+                        static_cast<int64_t>(w.g) * p.n + static_cast<int64_t>(w.n_tile) * 256;
+#pragma unroll
+                    for (int j = 0; j < L::kKbPerStage; ++j) {
+                        const int kb = kb0 + j;
+                        const uint32_t slot = s * L::kKbPerStage + j;
+                        const uint32_t sfa = sbase + L::kOffSfa + slot * L::kSfaBytes;
+                        const uint32_t sfb = sbase + L::kOffSfb + slot * L::kSfbBytes;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int r = q * 32 + lane;
+                            const int64_t m = static_cast<int64_t>(w.m_base) + r;
+                            const bool in = m < p.rows && kb < KB;
+                            const uint8_t* src = sa8 + sa_goff + m * (p.k >> 5) + kb * 8;
+#pragma unroll
+                            for (int wd = 0; wd < 2; ++wd)
+                                cp_async_4(sfa + wd * 512 + lane * 16 + q * 4, in ? src + 4 * wd : sa8,
+                                           in ? 4u : 0u);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int nr = q * 32 + lane;   // row of the unit's 256-row B tile
+                            const bool in = kb < KB;
+                            const uint8_t* src = sb8 + (brow0 + nr) * (p.k >> 5) + kb * 8;
+#pragma unroll
+                            for (int wd = 0; wd < 2; ++wd)
+                                cp_async_4(sfb + (2 * wd + (q >> 2)) * 512 + lane * 16 + (q & 3) * 4,
+                                           in ? src + 4 * wd : sb8, in ? 4u : 0u);
+                        }
+                    }
+                    cp_async_mbar_arrive_noinc(bar_sf_raw(s));
+                } else if (is_a) {
                     // raw scales of the stage's K blocks (zero beyond K and past the rows)
 #pragma unroll
                     for (int j = 0; j < L::kKbPerStage; ++j) {
@@ -618,6 +668,33 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         if (kb >= KB) break;
                         const int slot = s * L::kKbPerStage + j;
                         const uint32_t sf_col = 256 + slot * L::kSfColsPerKb;
+                        if constexpr (kMx) {
+                            // SFA words 0, 1 -> columns +0, +4; SFB (word, N half) -> +8 + 4 * (2w + h)
+#pragma unroll
+                            for (int m = 0; m < 2; ++m)
+                                tc_cp_pair_32x128b_warpx4(
+                                    tmem_base + sf_col + 4 * m,
+                                    make_desc_sf(sbase + L::kOffSfa + slot * L::kSfaBytes + 512 * m));
+#pragma unroll
+                            for (int m = 0; m < 4; ++m)
+                                tc_cp_pair_32x128b_warpx4(
+                                    tmem_base + sf_col + 8 + 4 * m,
+                                    make_desc_sf(sbase + L::kOffSfb + slot * L::kSfbBytes + 512 * m));
+                            const uint64_t adesc = make_desc_sw128(sbase + L::kOffA + s * L::kAStageBytes +
+                                                                   j * L::kTileBytes);
+                            const uint64_t bdesc = make_desc_sw128(sbase + L::kOffB + s * L::kBStageBytes +
+                                                                   j * L::kTileBytes);
+                            // MMA k covers elements 64k..64k+63 of the block: scale word k / 2,
+                            // bytes 2 (k % 2) and 2 (k % 2) + 1 (the instruction's scale id)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc_mma_pair_mxf4(tmem_base, adesc + 2u * k, bdesc + 2u * k,
+                                                 (k & 1) ? kIdescMx2 : kIdescMx0,
+                                                 tmem_base + sf_col + 4 * (k >> 1),
+                                                 tmem_base + sf_col + 8 + 8 * (k >> 1),
+                                                 (ks > pc.ks0 || j > 0 || k > 0) ? 1u : 0u);
+                            continue;
+                        }
                         tc_cp_pair_32x128b_warpx4(
                             tmem_base + sf_col, make_desc_sf(sbase + L::kOffSfa + slot * L::kSfaBytes));
                         tc_cp_pair_32x128b_warpx4(
@@ -667,7 +744,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     break;
                 }
 #pragma unroll
-                for (int j = 0; j < L::kKbPerStage; ++j) {
+                for (int j = 0; j < (kMx ? 0 : L::kKbPerStage); ++j) {
                     const int slot = s * L::kKbPerStage + j;
                     const uint32_t* raw = reinterpret_cast<const uint32_t*>(
                         smem + L::kOffSaRaw + slot * L::kSaRawBytes);

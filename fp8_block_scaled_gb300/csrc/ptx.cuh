@@ -352,6 +352,22 @@ __device__ __forceinline__ void tc_mma_pair_mxf8(uint32_t d_tmem, uint64_t a_des
         : "memory");
 }
 
+// Pair MMA on MXFP4 operands: packed E2M1 A and B (K = 64 per instruction, 32
+// bytes per row), one E8M0 scale per 32 elements (scale_vec::2X: two scale
+// bytes per row, chosen within the 32-bit tensor-memory word by the scale ids
+// of the instruction descriptor).
+__device__ __forceinline__ void tc_mma_pair_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa_tmem,
+                                                 uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Pair MMA without block scaling (kind::f8f6f4): D[tmem] (+)= A * B over K = 32.
 __device__ __forceinline__ void tc_mma_pair_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                uint32_t idesc, uint32_t accumulate) {
@@ -407,6 +423,14 @@ __device__ __forceinline__ uint64_t make_desc_sf(uint32_t saddr) {
 // (format code 0 in bits 7-9 and 10-12), both K-major (bits 15/16 = 0),
 // N>>3 in bits 17-22, UE8M0 scale type (bit 23 = 1), M>>4 in bits 24-28,
 // scale-factor byte selectors for B (bits 4-5) and A (bits 29-30) = 0.
+// Block-scaled instruction descriptor for kind::mxf4: E2M1 A and B (format 1 of
+// that kind, bits 7-9 and 10-12), UE8M0 scales (bit 23), N >> 3 at bit 17,
+// M >> 4 at bit 24, the scale-byte ids of A (bits 29-30) and B (bits 4-5).
+__host__ __device__ constexpr uint32_t make_idesc_mxf4(int m, int n, uint32_t sf_id) {
+    return (sf_id << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24) | (sf_id << 29);
+}
+
 __host__ __device__ constexpr uint32_t make_idesc_mxf8(int m, int n) {
     return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
            (static_cast<uint32_t>(m >> 4) << 24);

@@ -216,6 +216,37 @@ int gemm_grouped_masked_fp32_scales(const void* a, const float* scale_a, int sa_
                                     int64_t k, void* stream);
 
 /*
+ * MXFP4 (a4w4) grouped GEMM: both operands in the OCP Microscaling FP4
+ * format -- E2M1 elements (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) with one
+ * E8M0 scale byte 2^(e - 127) per 32 consecutive elements along K -- the MoE
+ * GEMM format of "flydsl mxfp4 a4w4 MoE: bring gemm1/gemm2 to parity with the
+ * HIP backend" (Summary).  D[r, n] = sum over 32-element blocks j of
+ * 2^(sa[r,j]-127) * 2^(sb[g,n,j]-127) * sum_{k in j} A[r,k] * B[g,n,k], fp32
+ * accumulation (tcgen05.mma kind::mxf4, scales applied by the tensor core).
+ *
+ *   a        packed E2M1 [m_sum, k/2] (contiguous) or [num_groups, m_max, k/2]
+ *            (masked); element 2i in the low nibble of byte i; 16-byte aligned
+ *   scale_a  E8M0 bytes [m_sum, k/32] or [num_groups, m_max, k/32]; 4-byte aligned
+ *   b        packed E2M1 [num_groups, n, k/2], 16-byte aligned
+ *   scale_b  E8M0 bytes [num_groups, n, k/32] (one per row of B and 32-element
+ *            block), 4-byte aligned
+ *   d        out_dtype [m_sum, n] or [num_groups, m_max, n], 32-byte aligned
+ *   n % 256 == 0, k % 256 == 0; contiguous: m_sum <= 507904 rows, num_groups
+ *   < 2^18.  grouped_layout / masked_m / expected_m as for the E4M3 variants.
+ * Runs on the CTA-pair kernel (with the stream-K tail for the contiguous
+ * variant).
+ */
+int gemm_grouped_contiguous_mxfp4(const void* a, const uint8_t* scale_a, const void* b,
+                                  const uint8_t* scale_b, const int32_t* grouped_layout, void* d,
+                                  int out_dtype, int64_t m_sum, int64_t n, int64_t k,
+                                  int64_t num_groups, void* stream);
+
+int gemm_grouped_masked_mxfp4(const void* a, const uint8_t* scale_a, const void* b,
+                              const uint8_t* scale_b, const int32_t* masked_m, int64_t expected_m,
+                              void* d, int out_dtype, int64_t num_groups, int64_t m_max,
+                              int64_t n, int64_t k, void* stream);
+
+/*
  * Contiguous grouped GEMM that allocates no device memory.  (No counterpart on
  * the pages: an addition for callers that may not call cudaMalloc -- for
  * example code that runs under a memory pool or allocator that owns all device

@@ -68,6 +68,10 @@ CONFIGS: Dict[str, dict] = {
     "c8_fp32scales_contig_g8_m1024_n2048_k7168": dict(
         variant="contiguous", G=8, N=2048, K=7168, out=OUT_BF16, sa_layout=SA_KM,
         sizes=("fixed", 1024), seed=8, scale_kind="fp32"),
+    # workload 2's shape with both operands in MXFP4 (E2M1, E8M0 per 32 elements)
+    "c9_mxfp4_contig_g8_m1024_n2048_k7168": dict(
+        variant="contiguous", G=8, N=2048, K=7168, out=OUT_BF16, sa_layout=SA_MK,
+        sizes=("fixed", 1024), seed=9, scale_kind="mxfp4"),
 }
 
 
@@ -116,6 +120,40 @@ def quantize_b_blocks(x: torch.Tensor, pow2: bool = True):
     s = _block_scale(amax, pow2)
     q = (xb / s[:, None, :, None]).to(torch.float8_e4m3fn).view(torch.uint8).reshape(n, k)
     return q, s
+
+
+# E2M1 rounding boundaries: midpoints between neighbouring magnitudes
+# 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7)
+_E2M1_MIDS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
+def quantize_mxfp4(x: torch.Tensor):
+    """[R, K] fp32 -> (packed E2M1 codes uint8 [R, K/2], E8M0 scale bytes uint8 [R, K/32]).
+
+    Reading of the OCP Microscaling conversion for MXFP4: per block of 32
+    elements along K the shared exponent is floor(log2 amax) - 2 (2 being the
+    largest E2M1 exponent; amax at least 1e-4), the scale is 2^that, and each
+    element x / scale goes to the nearest E2M1 value, ties to the even
+    mantissa, magnitudes above 6 saturating to 6.  Element 2i lands in the low
+    nibble of byte i.
+    """
+    r, k = x.shape
+    if k % 32:
+        raise ValueError("K must be a multiple of 32")
+    xb = x.float().reshape(r, k // 32, 32)
+    amax = xb.abs().amax(dim=2).clamp(min=AMAX_FLOOR).contiguous()
+    e = ((amax.view(torch.int32) >> 23) & 0xFF) - 127        # floor(log2 amax), amax normal
+    se = (e - 2).clamp(-127, 127)
+    scale = torch.ldexp(torch.ones_like(amax), se)
+    y = xb / scale.unsqueeze(2)                               # exact: power-of-two scale
+    mag = y.abs()
+    mids = torch.tensor(_E2M1_MIDS, dtype=torch.float32, device=x.device)
+    idx = torch.bucketize(mag, mids)                          # mids[i-1] < mag <= mids[i] -> i
+    tie = (mag == mids[idx.clamp(max=len(_E2M1_MIDS) - 1)]) & (idx % 2 == 1)
+    idx = idx + tie.to(idx.dtype)
+    codes = (idx | (torch.signbit(y).to(idx.dtype) << 3)).to(torch.uint8).reshape(r, k)
+    packed = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    return packed.contiguous(), (se + 127).to(torch.uint8)
 
 
 def _sub_seed(seed: int, tag: int, g: int) -> int:
@@ -172,7 +210,7 @@ class Problem:
     row_offsets: Optional[List[int]] = None        # contiguous: first row of each group
     pad_multiple: int = 128
     epilogue: str = ""    # "" (bf16/f16 D) or "silu_mul_quant" (E4M3 codes + scales of SiLU(gate)*up)
-    scale_kind: str = "ue8m0"  # "ue8m0" (power-of-two scales) or "fp32" (amax / 448 as is)
+    scale_kind: str = "ue8m0"  # "ue8m0" / "fp32" (E4M3 with such scales) or "mxfp4"
 
     @property
     def KB(self) -> int:
@@ -187,6 +225,11 @@ class Problem:
     def valid_rows(self) -> int:
         return int(sum(self.group_sizes))
 
+    @property
+    def is_mx(self) -> bool:
+        """MXFP4 operands: packed E2M1 [.., K/2] with E8M0 bytes [.., K/32]."""
+        return self.scale_kind == "mxfp4"
+
     def flops(self) -> float:
         return 2.0 * self.valid_rows * self.N * self.K
 
@@ -197,6 +240,10 @@ class Problem:
         b = used * self.N * self.K
         sa = self.valid_rows * self.KB * 4
         sb = used * (self.N // 128) * self.KB * 4
+        if self.is_mx:   # half a byte per element, one scale byte per 32 along K (A and B rows)
+            a, b = a // 2, b // 2
+            sa = self.valid_rows * (self.K // 32)
+            sb = used * self.N * (self.K // 32)
         d = self.valid_rows * self.N * out_bytes
         if self.epilogue == "silu_mul_quant":
             # N/2 code bytes and N/256 fp32 scales per row
@@ -261,8 +308,12 @@ def make_problem(variant: str, G: int, N: int, K: int, group_sizes, *, out_dtype
     computes or stores them is caught.  scale_kind "fp32" keeps each block's
     scale at amax / 448 instead of rounding it up to a power of two.
     """
-    if scale_kind not in ("ue8m0", "fp32"):
+    if scale_kind not in ("ue8m0", "fp32", "mxfp4"):
         raise ValueError(f"unknown scale_kind {scale_kind!r}")
+    if scale_kind == "mxfp4":
+        return _make_problem_mx(variant, G, N, K, group_sizes, out_dtype=out_dtype, seed=seed,
+                                M_max=M_max, pad_multiple=pad_multiple, device=device, name=name,
+                                tail_rows=tail_rows)
     pow2 = scale_kind == "ue8m0"
     sizes = [int(s) for s in group_sizes]
     if len(sizes) != G:
@@ -325,6 +376,52 @@ def make_problem(variant: str, G: int, N: int, K: int, group_sizes, *, out_dtype
     raise ValueError(f"unknown variant {variant!r}")
 
 
+def _make_problem_mx(variant, G, N, K, group_sizes, *, out_dtype, seed, M_max, pad_multiple,
+                     device, name, tail_rows) -> Problem:
+    """make_problem for MXFP4 operands (same data draws, quantize_mxfp4)."""
+    sizes = [int(s) for s in group_sizes]
+    if len(sizes) != G:
+        raise ValueError("one size per group")
+    if K % 256:
+        raise ValueError("MXFP4 workloads need K % 256 == 0")
+    b = torch.empty((G, N, K // 2), dtype=torch.uint8, device=device)
+    sb = torch.empty((G, N, K // 32), dtype=torch.uint8, device=device)
+    for g in range(G):
+        b[g], sb[g] = quantize_mxfp4(_randn((N, K), _sub_seed(seed, 2, g), device))
+    common = dict(name=name, variant=variant, G=G, N=N, K=K, out_dtype=out_dtype,
+                  sa_layout=SA_MK, seed=seed, group_sizes=sizes, ld_sa=K // 32, b=b, sb=sb,
+                  scale_kind="mxfp4")
+    if variant == "contiguous":
+        offsets = [0]
+        for m in sizes:
+            offsets.append(offsets[-1] + _round_up(m, pad_multiple) if m > 0 else offsets[-1])
+        m_sum = offsets[-1] + tail_rows
+        a = torch.empty((m_sum, K // 2), dtype=torch.uint8, device=device)
+        sa = torch.empty((m_sum, K // 32), dtype=torch.uint8, device=device)
+        layout = torch.full((m_sum,), -1, dtype=torch.int32, device=device)
+        for g in range(G):
+            lo, hi = offsets[g], offsets[g + 1]
+            if hi > lo:
+                a[lo:hi], sa[lo:hi] = quantize_mxfp4(_randn((hi - lo, K), _sub_seed(seed, 1, g),
+                                                            device))
+                layout[lo:lo + sizes[g]] = g
+        if tail_rows:
+            a[offsets[-1]:], sa[offsets[-1]:] = quantize_mxfp4(
+                _randn((tail_rows, K), _sub_seed(seed, 3, 0), device))
+        return Problem(a=a, sa=sa, grouped_layout=layout, row_offsets=offsets,
+                       pad_multiple=pad_multiple, **common)
+    if variant == "masked":
+        if M_max <= 0 or max(sizes) > M_max:
+            raise ValueError("masked: need 0 < max(masked_m) <= M_max")
+        a = torch.empty((G, M_max, K // 2), dtype=torch.uint8, device=device)
+        sa = torch.empty((G, M_max, K // 32), dtype=torch.uint8, device=device)
+        for g in range(G):
+            a[g], sa[g] = quantize_mxfp4(_randn((M_max, K), _sub_seed(seed, 1, g), device))
+        mm = torch.tensor(sizes, dtype=torch.int32, device=device)
+        return Problem(a=a, sa=sa, masked_m=mm, M_max=M_max, **common)
+    raise ValueError(f"unknown variant {variant!r}")
+
+
 def make_config(name: str, device="cpu") -> Problem:
     """One of the named workloads of CONFIGS."""
     c = CONFIGS[name]
@@ -360,6 +457,6 @@ def sample_rows(p: Problem, per_group: int = 32, seed: int = 0):
             np.array(sorted(set(untouched)), dtype=np.int64))
 
 
-__all__ = ["CONFIGS", "Problem", "make_problem", "make_config", "quantize_a_blocks",
+__all__ = ["CONFIGS", "Problem", "make_problem", "make_config", "quantize_a_blocks", "quantize_mxfp4",
            "quantize_b_blocks", "ceil_to_ue8m0_f32", "draw_group_sizes", "sample_rows",
            "SA_MK", "SA_KM", "OUT_BF16", "OUT_F16"]

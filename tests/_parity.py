@@ -22,6 +22,10 @@ import synth
 SENTINEL = 0x7FA5  # a NaN in both bf16 and f16
 CALC_DIFF_ORACLE = 1e-5
 CALC_DIFF_FP32 = 1e-3
+# MXFP4 operands carry one mantissa bit: rounding each operand to E2M1 costs
+# about 10% relative rms error, so calc_diff against the pre-quantisation fp32
+# product is about 0.5 * (0.14)^2 ~= 0.01; the check allows 5x that.
+CALC_DIFF_FP32_MX = 5e-2
 REL_TOL = 2.0 ** -7
 RMS_TOL = 1e-2
 
@@ -40,6 +44,16 @@ def run_gpu(p, d=None, stream=None):
     if d is None:
         d = torch.full(shape, SENTINEL, dtype=torch.int16 if SENTINEL < 0x8000 else torch.int32,
                        device=p.a.device).view(out_torch_dtype(p))
+    if p.is_mx:
+        if p.variant == "contiguous":
+            fb.gemm_grouped_contiguous_mxfp4(p.a, p.sa, p.b, p.sb, d, p.grouped_layout,
+                                             stream=stream)
+        else:
+            fb.gemm_grouped_masked_mxfp4(p.a, p.sa, p.b, p.sb, d, p.masked_m, stream=stream)
+        torch.cuda.synchronize()
+        err = fb.device_error()
+        assert err == 0, f"device error word {err:#x}"
+        return d.view(torch.int16).reshape(-1, p.N).cpu().numpy().view(np.uint16)
     sa = p.sa_mk_view()
     promote = p.scale_kind == "fp32"   # arbitrary fp32 scales: the software-promotion kernel
     if p.variant == "contiguous":
@@ -60,6 +74,13 @@ def oracle_rows(p, rows):
     b = p.b.cpu().numpy()
     sa = p.sa.cpu().numpy()
     sb = p.sb.cpu().numpy()
+    if p.is_mx:
+        if p.variant == "contiguous":
+            acc, valid, _ = oracle.mxfp4_contiguous(a, sa, b, sb, p.grouped_layout.cpu().numpy(),
+                                                    rows=rows)
+        else:
+            acc, valid, _ = oracle.mxfp4_masked(a, sa, b, sb, p.masked_m.cpu().numpy(), rows=rows)
+        return acc, valid
     if p.variant == "contiguous":
         acc, valid, _ = oracle.grouped_contiguous(a, sa, p.sa_layout, b, sb,
                                                   p.grouped_layout.cpu().numpy(), rows=rows,
@@ -108,7 +129,8 @@ def compare(p, bits, rows, untouched=(), check_fp32=True):
     if check_fp32:
         ref32 = fp32_reference_rows(p, rows)
         cd32 = oracle.calc_diff(got, ref32)
-        assert cd32 <= CALC_DIFF_FP32, f"calc_diff vs fp32 {cd32:.3e}"
+        assert cd32 <= (CALC_DIFF_FP32_MX if p.is_mx else CALC_DIFF_FP32), \
+            f"calc_diff vs fp32 {cd32:.3e}"
         stats["calc_diff_fp32"] = cd32
     untouched = np.asarray(untouched, dtype=np.int64)
     if untouched.size:

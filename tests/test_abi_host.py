@@ -224,3 +224,34 @@ def test_fp32_scales_masked_rejects_and_empty(lib):
         assert call(**bad) == INVALID, bad
     assert call(m_max=0, a=0) == OK
     assert _fp32s(m_sum=0, a=0, d=0) == OK
+
+
+def _mx(**kw):
+    args = dict(a=P, sa=P, b=P, sb=P, lay=P, d=P, out=0, m_sum=256, n=256, k=256, g=2)
+    args.update(kw)
+    return _binding.gemm_grouped_contiguous_mxfp4_raw(
+        args["a"], args["sa"], args["b"], args["sb"], args["lay"], args["d"], args["out"],
+        args["m_sum"], args["n"], args["k"], args["g"], 0)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(k=128),                 # K blocks of 128 packed bytes: k % 256 == 0
+    dict(n=384), dict(d=P + 16), dict(a=P + 8), dict(sa=P + 2), dict(sb=P + 1),
+    dict(a=0), dict(sa=0), dict(lay=0), dict(out=3), dict(g=0),
+    dict(m_sum=507904 + 128),    # MX pair-list limit
+])
+def test_mxfp4_rejects(lib, bad):
+    assert _mx(**bad) == INVALID
+
+
+def test_mxfp4_masked_rejects_and_empty(lib):
+    def call(**kw):
+        args = dict(a=P, sa=P, b=P, sb=P, mm=P, d=P, out=0, g=2, m_max=64, n=256, k=256)
+        args.update(kw)
+        return _binding.gemm_grouped_masked_mxfp4_raw(
+            args["a"], args["sa"], args["b"], args["sb"], args["mm"], 0, args["d"], args["out"],
+            args["g"], args["m_max"], args["n"], args["k"], 0)
+    for bad in (dict(k=128), dict(n=384), dict(mm=0), dict(d=P + 16), dict(g=1025)):
+        assert call(**bad) == INVALID, bad
+    assert call(m_max=0, a=0) == OK
+    assert _mx(m_sum=0, a=0, d=0) == OK

@@ -86,3 +86,33 @@ def test_sample_rows_cover_group_edges():
         assert p.group_of_row(int(r))[0] >= 0
     for r in u:
         assert p.group_of_row(int(r))[0] == -1
+
+
+def test_mxfp4_quantiser_invariants():
+    """Reading of the OCP MX conversion: per 32-element block the E8M0 byte is
+    floor(log2 amax) - 2 + 127, elements are the nearest E2M1 values of x / scale
+    (ties to the even code), saturating at 6."""
+    import oracle
+    from synth.inputs import quantize_mxfp4
+
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(16, 256, generator=g) * torch.logspace(-3, 3, 16).unsqueeze(1)
+    x[3] = 0.0
+    packed, sc = quantize_mxfp4(x)
+    assert packed.shape == (16, 128) and sc.shape == (16, 8)
+    codes = torch.stack([packed & 0xF, packed >> 4], dim=-1).reshape(16, 256).numpy()
+    vals = oracle.e2m1_decode(codes)
+    scale = np.ldexp(1.0, sc.numpy().astype(np.int64) - 127)
+    xb = x.double().numpy().reshape(16, 8, 32)
+    amax = np.maximum(np.abs(xb).max(axis=2), 1e-4)
+    assert np.array_equal(sc.numpy().astype(np.int64) - 127, np.floor(np.log2(amax)) - 2)
+    y = xb / scale[..., None]
+    deq = vals.reshape(16, 8, 32)
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    # nearest representable magnitude (saturating), compared by distance
+    best = np.abs(np.abs(y)[..., None] - grid).min(axis=-1)
+    assert np.allclose(np.abs(np.abs(deq) - np.minimum(np.abs(y), 6.0)),
+                       np.minimum(best, np.abs(np.minimum(np.abs(y), 6.0) - np.abs(deq))))
+    assert np.all(np.abs(np.abs(deq) - np.abs(y)) <= np.maximum(best, np.abs(y) - 6.0) + 1e-12)
+    assert np.all((deq == 0) | (np.sign(deq) == np.sign(y)))
+    assert np.all(codes[3] == 0)

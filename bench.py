@@ -385,35 +385,62 @@ def bench_ours(args):
 
 
 def bench_e2e(fb, p, dev, steps):
-    """Same metric through the public API, inputs in pinned host memory: each
-    step copies the inputs host->device, runs the GEMM and reads D back."""
+    """Same metric through the public API, inputs in pinned host memory: every
+    step copies its inputs host->device, runs the GEMM and reads its result back.
+
+    The steps are pipelined the way a serving loop would run them: two device
+    copies of the inputs and of the result, the host->device copies of step i+1
+    on one stream while step i computes on a second and its result returns on a
+    third, so the two copy directions and the GEMM overlap.  Every step's copies
+    are inside the timed region."""
     rowinfo = p.grouped_layout if p.variant == "contiguous" else p.masked_m
     host = [t.cpu().pin_memory() for t in (p.a, p.sa, p.b, p.sb, rowinfo)]
-    devb = [torch.empty_like(t, device=dev) for t in host]
-    d, d_dev = alloc_out(p, dev)
+    sets = [[torch.empty_like(t, device=dev) for t in host] for _ in range(2)]
+    outs = [alloc_out(p, dev) for _ in range(2)]
     _, d_host = alloc_out(p, dev, pinned=True)
+    s_in, s_gemm, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_gemm = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
     def sa_view(sa):
         if p.sa_layout == 0:
             return sa
         return sa[:, : p.rows].t() if p.variant == "contiguous" else sa[:, :, : p.M_max].transpose(1, 2)
 
-    def step():
-        for h, g in zip(host, devb):
-            g.copy_(h, non_blocking=True)
-        run_once(fb, p, devb[0], sa_view(devb[1]), devb[2], devb[3], devb[4], d)
-        for h, g in zip(d_host, d_dev):
-            h.copy_(g, non_blocking=True)
+    def step(i):
+        b = i % 2
+        s_in.wait_event(ev_gemm[b])          # the GEMM that last read input set b is done
+        with torch.cuda.stream(s_in):
+            for h, g in zip(host, sets[b]):
+                g.copy_(h, non_blocking=True)
+            ev_in[b].record(s_in)
+        s_gemm.wait_event(ev_in[b])
+        s_gemm.wait_event(ev_out[b])         # result buffer b has been read back
+        with torch.cuda.stream(s_gemm):
+            x = sets[b]
+            run_once(fb, p, x[0], sa_view(x[1]), x[2], x[3], x[4], outs[b][0], stream=s_gemm)
+            ev_gemm[b].record(s_gemm)
+        s_out.wait_event(ev_gemm[b])
+        with torch.cuda.stream(s_out):
+            for h, g in zip(d_host, outs[b][1]):
+                h.copy_(g, non_blocking=True)
+            ev_out[b].record(s_out)
 
-    for _ in range(2):
-        step()
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize(dev)
+    cur = torch.cuda.current_stream(dev)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        step()
-    t1.record()
+    t0.record(cur)
+    for s in (s_in, s_gemm, s_out):
+        s.wait_stream(cur)
+    for i in range(steps):
+        step(i)
+    for s in (s_in, s_gemm, s_out):
+        cur.wait_stream(s)
+    t1.record(cur)
     torch.cuda.synchronize(dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
     return {"ms_per_step": t0.elapsed_time(t1) / steps, "h2d": h2d,

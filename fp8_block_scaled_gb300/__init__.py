@@ -17,6 +17,7 @@ software instead of by the tensor core); the ``*_mxfp4`` entry points take both
 operands in MXFP4 (E2M1 with E8M0 scales per 32 elements).
 """
 from ._binding import (  # noqa: F401
+    DEBUG_STALL_MMA,
     DEVERR_BAD_GROUP,
     DEVERR_MASKED_M,
     DEVERR_MIXED_TILE,
@@ -49,5 +50,6 @@ from ._binding import (  # noqa: F401
     gemm_grouped_masked_silu_mul_quant_raw,
     lib_path,
     load,
+    set_debug_flags,
     status_string,
 )

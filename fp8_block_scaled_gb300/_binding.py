@@ -32,7 +32,8 @@ EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "gemm_grouped_conti
            "gemm_grouped_contiguous_silu_mul_quant", "gemm_grouped_masked_silu_mul_quant",
            "gemm_grouped_contiguous_fp32_scales", "gemm_grouped_masked_fp32_scales",
            "gemm_grouped_contiguous_mxfp4", "gemm_grouped_masked_mxfp4",
-           "fp8bs_device_error", "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version")
+           "fp8bs_device_error", "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version",
+           "fp8bs_set_debug_flags")
 
 _lib = None
 _lock = threading.Lock()
@@ -93,6 +94,8 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.fp8bs_status_string.restype = ctypes.c_char_p
         lib.fp8bs_clear_cache.argtypes = []
         lib.fp8bs_clear_cache.restype = _I
+        lib.fp8bs_set_debug_flags.argtypes = [ctypes.c_uint32]
+        lib.fp8bs_set_debug_flags.restype = _I
         lib.fp8bs_abi_version.argtypes = []
         lib.fp8bs_abi_version.restype = _I
         _lib = lib
@@ -441,6 +444,15 @@ def device_error(device: int = None) -> int:
     if st not in (0, 4):
         raise Fp8bsError(st, "fp8bs_device_error")
     return int(flags.value)
+
+
+DEBUG_STALL_MMA = 0x1
+
+
+def set_debug_flags(flags: int) -> None:
+    """Test hook (include/fp8bs.h): DEBUG_STALL_MMA makes later pair-kernel launches
+    time out and abort on purpose; 0 turns it off."""
+    _check(load().fp8bs_set_debug_flags(int(flags)), "fp8bs_set_debug_flags")
 
 
 def clear_cache() -> None:

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -204,6 +205,8 @@ int get_map3(int dev, const void* ptr, uint64_t inner, uint64_t outer, uint32_t 
 // follows in the stream is still finishing (its CTAs start on the SMs that
 // grid has already freed); after a grid that never signals, or after a
 // non-kernel stream operation, the launch is ordered as usual.
+std::atomic<uint32_t> g_debug_flags{0};  // fp8bs_set_debug_flags (tests only)
+
 inline void set_pdl(cudaLaunchAttribute& a) {
     a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     a.val.programmaticStreamSerializationAllowed = 1;
@@ -280,6 +283,7 @@ int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUt
                                                                    : st.max_clusters[attr_slot];
     if (pairs <= 0) return FP8BS_OK;
     GemmParams q = p;
+    q.debug_flags = g_debug_flags.load(std::memory_order_relaxed);
     int dev = 0;
     cudaGetDevice(&dev);
     SkWorkspace* w = kMasked ? nullptr : sk_workspace(dev, stream, 2 * st.max_clusters[attr_slot]);
@@ -473,6 +477,7 @@ int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUte
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
+    q.debug_flags = g_debug_flags.load(std::memory_order_relaxed);
     q.sk_partial = reinterpret_cast<float*>(nd.scratch);
     q.sk_flags = flags;
     q.sk_slots = kNoAllocSlots;
@@ -490,6 +495,12 @@ int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUte
 extern "C" {
 
 int fp8bs_abi_version(void) { return 1; }
+
+int fp8bs_set_debug_flags(uint32_t flags) {
+    if (flags & ~fp8bs::kDebugStallMma) return FP8BS_ERR_INVALID_ARG;
+    g_debug_flags.store(flags, std::memory_order_relaxed);
+    return FP8BS_OK;
+}
 
 const char* fp8bs_status_string(int status) {
     switch (status) {

@@ -47,6 +47,10 @@ constexpr uint32_t kErrTimeout = 0x1u;
 constexpr uint32_t kErrMaskedM = 0x2u;
 constexpr uint32_t kErrMixedTile = 0x4u;
 constexpr uint32_t kErrBadGroup = 0x8u;
+// GemmParams::debug_flags (test hook, 0 in normal use): the CTA-pair kernel's
+// MMA thread first waits on a barrier nothing arrives on, so its bounded wait
+// runs out and the launch takes the abort path.
+constexpr uint32_t kDebugStallMma = 0x1u;
 
 struct GemmParams {
     const float* sa;             // activation scales
@@ -72,6 +76,7 @@ struct GemmParams {
     int64_t qs_g_stride;         // masked: elements between groups; contiguous: 0
     int64_t qs_row_stride;       // elements between rows
     int64_t qs_col_stride;       // elements between 128-column blocks
+    uint32_t debug_flags;        // kDebug* test hooks, 0 in normal use
 };
 
 template <int BN>

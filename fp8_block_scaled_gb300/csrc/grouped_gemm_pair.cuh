@@ -648,6 +648,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             int s = 0;
             uint32_t ph = 0, acc_ph = 0;
             bool issued_any = false;
+            // test hook: phase 0 of the drain barrier completes only after a drain commit,
+            // which nothing has issued yet, so this wait runs out and the launch aborts
+            if ((p.debug_flags & kDebugStallMma) &&
+                !pair_wait(bar_drain, 0, abort_flag, peer_abort, p.err))
+                aborted = true;
             for (int pi = 0; !aborted; ++pi) {
                 const PairPiece pc = get_piece(pi);
                 if (pc.u < 0) break;

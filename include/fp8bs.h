@@ -294,6 +294,15 @@ const char* fp8bs_status_string(int status);
  * only kept. */
 int fp8bs_clear_cache(void);
 
+/* Test hook for the failure path (0 = off, the default).  FP8BS_DEBUG_STALL_MMA
+ * makes every later launch of the CTA-pair kernel wait, in its MMA thread, on
+ * a barrier nothing arrives on: the wait gives up after its time limit (4 s),
+ * the launch aborts (both CTAs of every pair stop, let their copies land,
+ * free tensor memory and exit) and FP8BS_DEVERR_TIMEOUT is recorded.  D is
+ * then undefined.  Returns FP8BS_ERR_INVALID_ARG for unknown bits. */
+#define FP8BS_DEBUG_STALL_MMA 0x1u
+int fp8bs_set_debug_flags(uint32_t flags);
+
 /* Library ABI version (1). */
 int fp8bs_abi_version(void);
 

@@ -40,7 +40,9 @@
  *    cudaMalloc on the first such call on that stream and keeps until exit.
  *    If that first call happens while the stream is being captured into a
  *    CUDA graph, or the allocation fails, the call runs without the split
- *    (same results, less balanced).  Launches on one stream share the
+ *    (same results, less balanced).  Calls can be captured into CUDA graphs;
+ *    a capture on a stream that has already run one call replays to the same
+ *    bits as the eager call.  Launches on one stream share the
  *    workspace safely; concurrent launches on different streams use
  *    different workspaces.
  *  - Rows that are not computed (grouped_layout == -1, or m >= masked_m[g])

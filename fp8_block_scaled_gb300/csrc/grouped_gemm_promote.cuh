@@ -246,12 +246,16 @@ grouped_gemm_promote_kernel(const __grid_constant__ CUtensorMap tmap_a,
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-            float scale = __ldg(sa_row) * __ldg(sb_blk);
+            // the scales of K block kb + 4 are fetched while block kb is promoted (a
+            // global load takes longer than one block's promotion)
+            auto sa_at = [&](int kb) { return kb < KB ? __ldg(sa_row + kb * p.sa_kb_stride) : 0.0f; };
+            auto sb_at = [&](int kb) { return kb < KB ? __ldg(sb_blk + kb) : 0.0f; };
+            float a0 = sa_at(0), a1 = sa_at(1), a2 = sa_at(2), a3 = sa_at(3);
+            float b0 = sb_at(0), b1 = sb_at(1), b2 = sb_at(2), b3 = sb_at(3);
             for (int kb = 0; kb < KB; ++kb) {
-                // the next block's scale is fetched while this block is promoted
-                const float next = kb + 1 < KB
-                                       ? __ldg(sa_row + (kb + 1) * p.sa_kb_stride) * __ldg(sb_blk + kb + 1)
-                                       : 0.0f;
+                const float scale = a0 * b0;
+                a0 = a1; a1 = a2; a2 = a3; a3 = sa_at(kb + 4);
+                b0 = b1; b1 = b2; b2 = b3; b3 = sb_at(kb + 4);
                 const uint32_t b = kc & 1u;
                 if (!pair_warp_wait(bar_p_full(b), (kc >> 1) & 1u, abort_flag, peer_abort,
                                     p.err)) {
@@ -272,7 +276,6 @@ grouped_gemm_promote_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 if (lane == 0) mbar_arrive_relaxed_cluster(mapa_shared(bar_p_empty(b), 0));
                 ++kc;
-                scale = next;
             }
             if (aborted) break;
             if (valid) {

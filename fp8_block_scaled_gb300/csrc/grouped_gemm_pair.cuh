@@ -571,46 +571,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     }
                     if (pf) tma_prefetch_3d(map, 0, prow, kp * L::kKbPerStage);
                 }
-                if (is_a && kMx) {
-                    // MXFP4: E8M0 bytes, [rows, K/32] for A (masked: per group, sa_g_stride
-                    // bytes apart) and [G*N, K/32] for B.  A K block
-                    // has 8 per row = two 4-byte words; word w of row r goes to lane r % 32,
-                    // column r / 32 of 32x128b matrix w (SFB: matrix 2w + n / 128), the
-                    // layout tcgen05.cp moves into tensor memory unchanged.
-                    const uint8_t* sa8 = reinterpret_cast<const uint8_t*>(p.sa);
-                    const uint8_t* sb8 = reinterpret_cast<const uint8_t*>(p.sb);
-                    const int64_t brow0 =
-                        static_cast<int64_t>(w.g) * p.n + static_cast<int64_t>(w.n_tile) * 256;
-#pragma unroll
-                    for (int j = 0; j < L::kKbPerStage; ++j) {
-                        const int kb = kb0 + j;
-                        const uint32_t slot = s * L::kKbPerStage + j;
-                        const uint32_t sfa = sbase + L::kOffSfa + slot * L::kSfaBytes;
-                        const uint32_t sfb = sbase + L::kOffSfb + slot * L::kSfbBytes;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int r = q * 32 + lane;
-                            const int64_t m = static_cast<int64_t>(w.m_base) + r;
-                            const bool in = m < p.rows && kb < KB;
-                            const uint8_t* src = sa8 + sa_goff + m * (p.k >> 5) + kb * 8;
-#pragma unroll
-                            for (int wd = 0; wd < 2; ++wd)
-                                cp_async_4(sfa + wd * 512 + lane * 16 + q * 4, in ? src + 4 * wd : sa8,
-                                           in ? 4u : 0u);
-                        }
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int nr = q * 32 + lane;   // row of the unit's 256-row B tile
-                            const bool in = kb < KB;
-                            const uint8_t* src = sb8 + (brow0 + nr) * (p.k >> 5) + kb * 8;
-#pragma unroll
-                            for (int wd = 0; wd < 2; ++wd)
-                                cp_async_4(sfb + (2 * wd + (q >> 2)) * 512 + lane * 16 + (q & 3) * 4,
-                                           in ? src + 4 * wd : sb8, in ? 4u : 0u);
-                        }
-                    }
-                    cp_async_mbar_arrive_noinc(bar_sf_raw(s));
-                } else if (is_a) {
+                if (is_a && !kMx) {
                     // raw scales of the stage's K blocks (zero beyond K and past the rows)
 #pragma unroll
                     for (int j = 0; j < L::kKbPerStage; ++j) {
@@ -736,6 +697,133 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             }
         }
         __syncwarp();
+    } else if (warp == 3 && kMx) {
+        // ============================================================ MXFP4 scale staging
+        // E8M0 bytes, [rows, K/32] for A (masked: per group, sa_g_stride bytes apart)
+        // and [G*N, K/32] for B.  A K block has 8 per row = two 4-byte words; word w of
+        // row r goes to lane r % 32, column r / 32 of 32x128b matrix w (SFB: matrix
+        // 2w + n / 128), the layout tcgen05.cp moves into tensor memory unchanged.  This
+        // warp issues a stage's copies as soon as the stage is free and signals the
+        // stage one step later, so two stages of scales are in flight while the
+        // producers issue only the operand boxes.
+        //
+        // When a scale row's stage slice (2 K blocks = 16 bytes) is 16-byte aligned
+        // (K % 512 == 0), each row is fetched with one 16-byte copy into row-major
+        // staging at the slot's own address, then rearranged in place: lane l fetches
+        // exactly the rows l + 32c (SFB: + 128h) whose 16-byte slots its rearranged
+        // words occupy, so the transpose is lane-local.  (4-byte copies straight into
+        // place issue four times as many memory requests, which bounded this path.)
+        const uint8_t* sa8 = reinterpret_cast<const uint8_t*>(p.sa);
+        const uint8_t* sb8 = reinterpret_cast<const uint8_t*>(p.sb);
+        const bool wide = (p.k & 511) == 0;
+        int s = 0, prev_s = -1;
+        uint32_t ph = 0, prev_ph = 0;
+        auto signal = [&](int st, uint32_t sph) {
+            if (!pair_warp_wait(bar_sf_raw(st), sph, abort_flag, peer_abort, p.err)) {
+                aborted = true;
+                return;
+            }
+            if (wide) {
+                uint4* sfa = reinterpret_cast<uint4*>(smem + L::kOffSfa +
+                                                      st * L::kKbPerStage * L::kSfaBytes);
+                uint4 r[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) r[c] = sfa[c * 32 + lane];
+                sfa[lane] = make_uint4(r[0].x, r[1].x, r[2].x, r[3].x);        // K block 0, word 0
+                sfa[32 + lane] = make_uint4(r[0].y, r[1].y, r[2].y, r[3].y);   // K block 0, word 1
+                sfa[64 + lane] = make_uint4(r[0].z, r[1].z, r[2].z, r[3].z);   // K block 1, word 0
+                sfa[96 + lane] = make_uint4(r[0].w, r[1].w, r[2].w, r[3].w);   // K block 1, word 1
+                uint4* sfb = reinterpret_cast<uint4*>(smem + L::kOffSfb +
+                                                      st * L::kKbPerStage * L::kSfbBytes);
+                // all eight rows first: the rearranged words of one half land on raw rows
+                // of the other
+                uint4 t[8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) t[h * 4 + c] = sfb[h * 128 + c * 32 + lane];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4* u = t + h * 4;
+                    // (K block, word, half) -> matrix K block * 4 + 2 word + half
+                    sfb[(0 * 4 + 0 + h) * 32 + lane] = make_uint4(u[0].x, u[1].x, u[2].x, u[3].x);
+                    sfb[(0 * 4 + 2 + h) * 32 + lane] = make_uint4(u[0].y, u[1].y, u[2].y, u[3].y);
+                    sfb[(1 * 4 + 0 + h) * 32 + lane] = make_uint4(u[0].z, u[1].z, u[2].z, u[3].z);
+                    sfb[(1 * 4 + 2 + h) * 32 + lane] = make_uint4(u[0].w, u[1].w, u[2].w, u[3].w);
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa_shared(bar_full(st), 0));
+        };
+        for (int pi = 0; !aborted; ++pi) {
+            const PairPiece pc = get_piece(pi);
+            if (pc.u < 0) break;
+            const PairUnit w = get_unit(pc.u);
+            const int64_t sa_goff = kMasked ? static_cast<int64_t>(w.g) * p.sa_g_stride : 0;
+            const int64_t brow0 =
+                static_cast<int64_t>(w.g) * p.n + static_cast<int64_t>(w.n_tile) * 256;
+            for (int ks = pc.ks0; ks < pc.ks1 && !aborted; ++ks) {
+                if (!pair_warp_wait(bar_empty(s), ph ^ 1u, abort_flag, peer_abort, p.err)) {
+                    aborted = true;
+                    break;
+                }
+                const int kb0 = ks * L::kKbPerStage;
+                if (wide) {
+                    // the stage's 16 bytes of every row (8 when its second K block is past K)
+                    const uint32_t nbytes = kb0 + 1 < KB ? 16u : 8u;
+                    const uint32_t sfa = sbase + L::kOffSfa + s * L::kKbPerStage * L::kSfaBytes;
+                    const uint32_t sfb = sbase + L::kOffSfb + s * L::kKbPerStage * L::kSfbBytes;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int r = c * 32 + lane;
+                        const int64_t m = static_cast<int64_t>(w.m_base) + r;
+                        const bool in = m < p.rows;
+                        cp_async_16(sfa + 16 * r, in ? sa8 + sa_goff + m * (p.k >> 5) + kb0 * 8 : sa8,
+                                    in ? nbytes : 0u);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int nr = q * 32 + lane;
+                        cp_async_16(sfb + 16 * nr, sb8 + (brow0 + nr) * (p.k >> 5) + kb0 * 8, nbytes);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < (wide ? 0 : L::kKbPerStage); ++j) {
+                    const int kb = kb0 + j;
+                    const uint32_t slot = s * L::kKbPerStage + j;
+                    const uint32_t sfa = sbase + L::kOffSfa + slot * L::kSfaBytes;
+                    const uint32_t sfb = sbase + L::kOffSfb + slot * L::kSfbBytes;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int r = q * 32 + lane;
+                        const int64_t m = static_cast<int64_t>(w.m_base) + r;
+                        const bool in = m < p.rows && kb < KB;
+                        const uint8_t* src = sa8 + sa_goff + m * (p.k >> 5) + kb * 8;
+#pragma unroll
+                        for (int wd = 0; wd < 2; ++wd)
+                            cp_async_4(sfa + wd * 512 + lane * 16 + q * 4, in ? src + 4 * wd : sa8,
+                                       in ? 4u : 0u);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int nr = q * 32 + lane;   // row of the unit's 256-row B tile
+                        const bool in = kb < KB;
+                        const uint8_t* src = sb8 + (brow0 + nr) * (p.k >> 5) + kb * 8;
+#pragma unroll
+                        for (int wd = 0; wd < 2; ++wd)
+                            cp_async_4(sfb + (2 * wd + (q >> 2)) * 512 + lane * 16 + (q & 3) * 4,
+                                       in ? src + 4 * wd : sb8, in ? 4u : 0u);
+                    }
+                }
+                cp_async_mbar_arrive_noinc(bar_sf_raw(s));
+                if (prev_s >= 0) signal(prev_s, prev_ph);
+                prev_s = s;
+                prev_ph = ph;
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+        }
+        if (!aborted && prev_s >= 0) signal(prev_s, prev_ph);
     } else if (warp == 3) {
         // ============================================================ scale converter
         int s = 0;

@@ -99,6 +99,14 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
                  : "memory");
 }
 
+// 16-byte cp.async (L2 only); bytes beyond src_bytes (0, 8 or 16) are written as zero.
+// dst and src must be 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
 // Arrive on `bar` once all of this thread's earlier cp.async copies have
 // landed; the arrival counts toward the barrier's expected count.
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {

@@ -268,8 +268,8 @@ grouped_gemm_promote_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     uint32_t v[16];
                     tc_ld_32x32b_x16_sync(trow + 256u * b + 16 * c, v);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        acc[16 * c + i] = fmaf(__uint_as_float(v[i]), scale, acc[16 * c + i]);
+                    for (int i = 0; i < 16; i += 2)
+                        fma2_scaled(acc[16 * c + i], acc[16 * c + i + 1], v[i], v[i + 1], scale);
                 }
                 // all reads of the buffer have completed (wait::ld): hand it back
                 tc_fence_before();

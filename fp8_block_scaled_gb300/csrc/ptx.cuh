@@ -178,6 +178,20 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
         : "memory");
 }
 
+// (a0, a1) = fma((x0, x1), s, (a0, a1)) with one packed two-lane fp32 FMA
+// (fma.rn.f32x2): each lane is an IEEE fused multiply-add rounded to nearest,
+// so the result is bit-identical to two fmaf calls in half the instructions.
+__device__ __forceinline__ void fma2_scaled(float& a0, float& a1, uint32_t x0, uint32_t x1, float s) {
+    asm("{\n\t.reg .b64 ra, rx, rs;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rx, {%2, %3};\n\t"
+        "mov.b64 rs, {%4, %4};\n\t"
+        "fma.rn.f32x2 ra, rx, rs, ra;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(x0), "r"(x1), "f"(s));
+}
+
 // Copy a 32-row x 128-bit matrix from shared memory into TMEM lanes 0-31 of
 // the target columns and broadcast it to the other three 32-lane quadrants.
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {

@@ -112,8 +112,9 @@ struct PairLayoutT {
     static_assert(256 + kStages * kKbPerStage * kSfColsPerKb <= kTmemCols, "TMEM budget");
     static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
     static_assert(kPairMaxTiles * 4 <= kStages * kAStageBytes, "prologue scratch");
-    static_assert(kPartChunks * kPartChunkBytes <= kStages * (kAStageBytes + kBStageBytes),
-                  "stream-K partial staging");
+    static_assert(kPartChunks == 4 && kAStageBytes == kPartChunkBytes &&
+                      kBStageBytes == kPartChunkBytes && kStages >= 2,
+                  "stream-K partial staging: chunks fill the A and B halves of two stages");
 };
 using PairLayout = PairLayoutT<false>;
 
@@ -529,6 +530,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint32_t op_off = is_a ? L::kOffA : L::kOffB;
         int s = 0;
         uint32_t ph = 0;
+        int last_kind = 0;
         for (int pi = 0; !aborted; ++pi) {
             const PairPiece pc = get_piece(pi);
             if (pc.u < 0) break;
@@ -600,6 +602,45 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     }
                     cp_async_mbar_arrive_noinc(bar_sf_raw(s));
                 }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            last_kind = pc.kind;
+        }
+        // The pair's last piece is the head of a split unit: copy the partial its tail
+        // published into the two stages after the last step as soon as their MMAs
+        // have completed (chunks 2j and 2j + 1 into the A and B halves of stage j),
+        // so that the copies overlap the last steps instead of following them.
+        if (is_a && last_kind == 1) {
+            const int slot = (pair_id + 1) * 2 + static_cast<int>(rank);
+            const float* src = p.sk_partial + static_cast<int64_t>(slot) * (128 * 256);
+            for (int j = 0; j < 2 && !aborted; ++j) {
+                if (!pair_warp_wait(bar_empty(s), ph ^ 1u, abort_flag, peer_abort, p.err)) {
+                    aborted = true;
+                    break;
+                }
+                if (lane == 0) {
+                    if (j == 0) {
+                        const uint64_t t0 = global_timer_ns();
+                        while (ld_acquire_gpu_u32(p.sk_flags + 2 * slot) < 4u) {
+                            if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+                                raise_error(p.err, kErrTimeout);
+                                break;
+                            }
+                        }
+                        // the copies are issued even after a time-out, so that no warp
+                        // waits for them in vain (the error is already recorded)
+                        fence_proxy_async_global();
+                    }
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = 2 * j + h;
+                        mbar_arrive_expect_tx(bar_part(c), L::kPartChunkBytes);
+                        bulk_load(sbase + (h ? L::kOffB + s * L::kBStageBytes
+                                             : L::kOffA + s * L::kAStageBytes),
+                                  src + c * (L::kPartChunkBytes / 4), L::kPartChunkBytes,
+                                  bar_part(c));
+                    }
+                }
+                __syncwarp();
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
         }
@@ -868,9 +909,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const int row_in_half = q * 32 + lane;
         const uint32_t empty_leader = mapa_shared(bar_tmem_empty, 0);
         uint32_t acc_ph = 0;
+        int steps_done = 0;  // pipeline steps of this CTA up to and including piece pi
         for (int pi = 0; !aborted; ++pi) {
             const PairPiece pc = get_piece(pi);
             if (pc.u < 0) break;
+            steps_done += pc.ks1 - pc.ks0;
             const PairUnit w = get_unit(pc.u);
             const int64_t m = static_cast<int64_t>(w.m_base) + row_in_half;
             bool valid = w.store;
@@ -976,32 +1019,19 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 if (lane == 0) atomicAdd(p.sk_flags + 2 * slot, 1u);
             } else {
-                // head (the pair's last piece; every MMA reading the stages has completed)
+                // head (the pair's last piece): the A producer has staged the partial of
+                // the unit's tail in the two stages after this CTA's last step, chunk c in
+                // the A (c even) or B (c odd) half of stage (last + 1 + c / 2) mod S
                 const int slot = (pair_id + 1) * 2 + static_cast<int>(rank);
-                if (warp == 4 && lane == 0) {
-                    const uint64_t t0 = global_timer_ns();
-                    while (ld_acquire_gpu_u32(p.sk_flags + 2 * slot) < 4u) {
-                        if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
-                            raise_error(p.err, kErrTimeout);
-                            break;
-                        }
-                    }
-                    // the copies are issued even after a time-out, so that no warp
-                    // waits for them in vain (the error is already recorded)
-                    fence_proxy_async_global();
-                    const float* src = p.sk_partial + static_cast<int64_t>(slot) * (128 * 256);
-#pragma unroll
-                    for (int c = 0; c < L::kPartChunks; ++c) {
-                        mbar_arrive_expect_tx(bar_part(c), L::kPartChunkBytes);
-                        bulk_load(sbase + L::kOffA + c * L::kPartChunkBytes,
-                                  src + c * (L::kPartChunkBytes / 4), L::kPartChunkBytes,
-                                  bar_part(c));
-                    }
-                }
+                auto part_chunk = [&](int c) {
+                    const int sc = (steps_done + (c >> 1)) % S;
+                    return reinterpret_cast<const float*>(
+                        smem + ((c & 1) ? L::kOffB + sc * L::kBStageBytes
+                                        : L::kOffA + sc * L::kAStageBytes));
+                };
                 if constexpr (kSwiglu) {
                     // partial column col of this row in the staged slot: chunk col / 64,
                     // column group (col % 64) / 8, [128 rows][8 columns] per group
-                    const float* part = reinterpret_cast<const float*>(smem + L::kOffA) + row_in_half * 8;
                     float h[128];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {  // 32 gate columns and the matching up columns
@@ -1021,15 +1051,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 break;
                             }
                         }
+                        // gate columns 32c.. are in chunk c / 2, the up columns in chunk 2 + c / 2
+                        const float* gpart = part_chunk(c >> 1) + row_in_half * 8;
+                        const float* upart = part_chunk(2 + (c >> 1)) + row_in_half * 8;
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
-                            const int gcol = 32 * c + i, ucol = 128 + 32 * c + i;
+                            const int col = (32 * c + i) & 63;
                             const float4 gp = *reinterpret_cast<const float4*>(
-                                part + (gcol >> 6) * (L::kPartChunkBytes / 4) +
-                                ((gcol & 63) >> 3) * (128 * 8) + (gcol & 7));
+                                gpart + (col >> 3) * (128 * 8) + (col & 7));
                             const float4 up = *reinterpret_cast<const float4*>(
-                                part + (ucol >> 6) * (L::kPartChunkBytes / 4) +
-                                ((ucol & 63) >> 3) * (128 * 8) + (ucol & 7));
+                                upart + (col >> 3) * (128 * 8) + (col & 7));
                             h[32 * c + i] = silu_f32(__uint_as_float(gv[i]) + gp.x) *
                                             (__uint_as_float(uv[i]) + up.x);
                             h[32 * c + i + 1] = silu_f32(__uint_as_float(gv[i + 1]) + gp.y) *
@@ -1056,9 +1087,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         break;
                     }
                     // chunk c: [8 column groups][128 rows][8 columns] fp32
-                    const float* part = reinterpret_cast<const float*>(
-                                            smem + L::kOffA + c * L::kPartChunkBytes) +
-                                        row_in_half * 8;
+                    const float* part = part_chunk(c) + row_in_half * 8;
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {

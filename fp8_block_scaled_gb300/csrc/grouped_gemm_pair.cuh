@@ -110,6 +110,7 @@ struct PairLayoutT {
     static constexpr int kSfColsPerKb = kMx ? 8 + 16 : 4 + 8;
     static constexpr int kTmemCols = 512;
     static_assert(256 + kStages * kKbPerStage * kSfColsPerKb <= kTmemCols, "TMEM budget");
+    static_assert(kKbPerStage <= 4, "E4M3 scale words hold one byte per K block of a stage");
     static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
     static_assert(kPairMaxTiles * 4 <= kStages * kAStageBytes, "prologue scratch");
     static_assert(kPartChunks == 4 && kAStageBytes == kPartChunkBytes &&
@@ -673,9 +674,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     for (int j = 0; j < L::kKbPerStage; ++j) {
                         const int kb = ks * L::kKbPerStage + j;
                         if (kb >= KB) break;
-                        const int slot = s * L::kKbPerStage + j;
-                        const uint32_t sf_col = 256 + slot * L::kSfColsPerKb;
                         if constexpr (kMx) {
+                            const int slot = s * L::kKbPerStage + j;
+                            const uint32_t sf_col = 256 + slot * L::kSfColsPerKb;
                             // SFA words 0, 1 -> columns +0, +4; SFB (word, N half) -> +8 + 4 * (2w + h)
 #pragma unroll
                             for (int m = 0; m < 2; ++m)
@@ -702,14 +703,21 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                                  (ks > pc.ks0 || j > 0 || k > 0) ? 1u : 0u);
                             continue;
                         }
-                        tc_cp_pair_32x128b_warpx4(
-                            tmem_base + sf_col, make_desc_sf(sbase + L::kOffSfa + slot * L::kSfaBytes));
-                        tc_cp_pair_32x128b_warpx4(
-                            tmem_base + sf_col + 4,
-                            make_desc_sf(sbase + L::kOffSfb + slot * L::kSfbBytes));
-                        tc_cp_pair_32x128b_warpx4(
-                            tmem_base + sf_col + 8,
-                            make_desc_sf(sbase + L::kOffSfb + slot * L::kSfbBytes + 512));
+                        // the stage's scale words (byte j for K block j) are copied once, with
+                        // its first K block, into the columns of the stage's first slot
+                        const int slot0 = s * L::kKbPerStage;
+                        const uint32_t sf0 = 256 + slot0 * L::kSfColsPerKb;
+                        if (j == 0) {
+                            tc_cp_pair_32x128b_warpx4(
+                                tmem_base + sf0, make_desc_sf(sbase + L::kOffSfa + slot0 * L::kSfaBytes));
+                            tc_cp_pair_32x128b_warpx4(
+                                tmem_base + sf0 + 4,
+                                make_desc_sf(sbase + L::kOffSfb + slot0 * L::kSfbBytes));
+                            tc_cp_pair_32x128b_warpx4(
+                                tmem_base + sf0 + 8,
+                                make_desc_sf(sbase + L::kOffSfb + slot0 * L::kSfbBytes + 512));
+                        }
+                        const uint32_t idesc_j = idesc_scale_ids(kIdesc, static_cast<uint32_t>(j));
                         const uint64_t adesc = make_desc_sw128(sbase + L::kOffA + s * L::kAStageBytes +
                                                                j * L::kTileBytes);
                         const uint64_t bdesc = make_desc_sw128(sbase + L::kOffB + s * L::kBStageBytes +
@@ -717,8 +725,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
                         for (int k = 0; k < kBK / kUmmaK; ++k) {
                             // the first MMA of a piece overwrites the accumulator
-                            tc_mma_pair_mxf8(tmem_base, adesc + 2u * k, bdesc + 2u * k, kIdesc,
-                                             tmem_base + sf_col, tmem_base + sf_col + 4,
+                            tc_mma_pair_mxf8(tmem_base, adesc + 2u * k, bdesc + 2u * k, idesc_j,
+                                             tmem_base + sf0, tmem_base + sf0 + 4,
                                              (ks > pc.ks0 || j > 0 || k > 0) ? 1u : 0u);
                         }
                     }
@@ -877,23 +885,32 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     aborted = true;
                     break;
                 }
+                if constexpr (!kMx) {
+                    // One scale word per row (SFA) or column chunk (SFB) and stage: byte j
+                    // is the UE8M0 scale of the stage's K block j, and the MMAs of K block j
+                    // select byte j through the instruction's scale ids, so a stage needs
+                    // one set of scale copies instead of one per K block.
+                    const int slot0 = s * L::kKbPerStage;
+                    auto word = [&](int off_raw, int raw_bytes, int i) {
+                        uint32_t w = 0;
 #pragma unroll
-                for (int j = 0; j < (kMx ? 0 : L::kKbPerStage); ++j) {
-                    const int slot = s * L::kKbPerStage + j;
-                    const uint32_t* raw = reinterpret_cast<const uint32_t*>(
-                        smem + L::kOffSaRaw + slot * L::kSaRawBytes);
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t* raw = reinterpret_cast<const uint32_t*>(
+                                smem + off_raw + (slot0 + j % L::kKbPerStage) * raw_bytes);
+                            w |= ((raw[i] >> 23) & 0xFFu) << (8 * j);
+                        }
+                        return w;
+                    };
                     uint4 wv;
-                    wv.x = ue8m0_x4(raw[lane]);
-                    wv.y = ue8m0_x4(raw[32 + lane]);
-                    wv.z = ue8m0_x4(raw[64 + lane]);
-                    wv.w = ue8m0_x4(raw[96 + lane]);
-                    *reinterpret_cast<uint4*>(smem + L::kOffSfa + slot * L::kSfaBytes + 16 * lane) = wv;
-                    const uint32_t* sbraw = reinterpret_cast<const uint32_t*>(
-                        smem + L::kOffSbRaw + slot * L::kSbRawBytes);
+                    wv.x = word(L::kOffSaRaw, L::kSaRawBytes, lane);
+                    wv.y = word(L::kOffSaRaw, L::kSaRawBytes, 32 + lane);
+                    wv.z = word(L::kOffSaRaw, L::kSaRawBytes, 64 + lane);
+                    wv.w = word(L::kOffSaRaw, L::kSaRawBytes, 96 + lane);
+                    *reinterpret_cast<uint4*>(smem + L::kOffSfa + slot0 * L::kSfaBytes + 16 * lane) = wv;
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        const uint32_t v = ue8m0_x4(sbraw[c]);
-                        *reinterpret_cast<uint4*>(smem + L::kOffSfb + slot * L::kSfbBytes + 512 * c +
+                        const uint32_t v = word(L::kOffSbRaw, L::kSbRawBytes, c);
+                        *reinterpret_cast<uint4*>(smem + L::kOffSfb + slot0 * L::kSfbBytes + 512 * c +
                                                   16 * lane) = make_uint4(v, v, v, v);
                     }
                 }

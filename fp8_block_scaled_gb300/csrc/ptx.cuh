@@ -453,6 +453,13 @@ __host__ __device__ constexpr uint32_t make_idesc_mxf4(int m, int n, uint32_t sf
            (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24) | (sf_id << 29);
 }
 
+// The scale-factor ids of a block-scaled instruction descriptor (bits 4-5 for B,
+// 29-30 for A): with scale_vec::1X they select which byte of each 32-bit scale
+// word in tensor memory the MMA uses.
+__host__ __device__ constexpr uint32_t idesc_scale_ids(uint32_t idesc, uint32_t id) {
+    return idesc | (id << 4) | (id << 29);
+}
+
 __host__ __device__ constexpr uint32_t make_idesc_mxf8(int m, int n) {
     return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
            (static_cast<uint32_t>(m >> 4) << 24);

@@ -22,32 +22,34 @@
 // most once, into a head [0, x) finished last by one pair and a tail [x, end)
 // finished first by the next pair.  Each epilogue warp of the tail writes its
 // rows of the fp32 partial accumulator to a scratch slot and counts itself in
-// the slot's ready word.  The head is always its pair's last piece, so once
-// its accumulator is complete the operand stages are idle: one thread of the
-// head waits (bounded) until all four tail warps have counted themselves,
-// copies the 128 KB slot into the stages with four bulk copies, and resets
-// the ready word for the next launch; every epilogue warp then adds the
-// partial chunk by chunk from shared memory.  Reading the partial with plain
-// loads instead left four dependent round trips to a remote L2 slice exposed
-// at the very end of the kernel.
+// the slot's ready word.  The head is always its pair's last piece, so the two
+// ring stages after its last step are never loaded again: the A producer waits
+// for their MMAs to release them, waits (bounded) until all four tail warps
+// have counted themselves, and copies the 128 KB slot into them with four
+// bulk copies that overlap the head's last steps; every epilogue warp then
+// adds the partial chunk by chunk from shared memory, and one resets the ready
+// word for the next launch.  Reading the partial with plain loads instead left
+// four dependent round trips to a remote L2 slice exposed at the very end of
+// the kernel.
 //
 // Operand staging: each pipeline stage holds two 128-K blocks, fetched with
 // one 3-D TMA box per operand (128 bytes x 128 rows x 2 blocks); the A and B
-// boxes are issued by two different warps.  The TMA engine completes the boxes
-// of one issuing warp one after another, so two issuers with 32 KB boxes move
-// an SM's 64 KB per stage about as fast as the MMAs consume it.
+// boxes are issued by two different warps.  One thread issues at most a few
+// million boxes a second whatever their size, so large boxes from two issuers
+// keep the issue rate well below that while 64 KB per stage is in flight.
 //
 // Warp roles per CTA (both CTAs run all roles except the MMA issue):
 //   warp 0  A producer: TMA of its 128 rows of A (completion counted on the
 //           leader's full barrier, which only the leader arms, for the bytes
 //           of both CTAs), cp.async of the raw fp32 scales
 //   warp 2  B producer (after allocating the pair's tensor memory)
-//   warp 3  scale converter: UE8M0 words in tcgen05.cp order, then an
-//           arrival on the leader's full barrier of the stage
+//   warp 3  scale converter: UE8M0 scale words in tcgen05.cp order, one word
+//           per row (SFA) or column chunk (SFB) and stage with byte j for the
+//           stage's K block j, then an arrival on the leader's full barrier
 //   warp 1  (leader only, one thread) tcgen05.cp / tcgen05.mma issue,
-//           commits multicast to both CTAs.  tcgen05.mma issue is nearly
-//           synchronous with the tensor pipe, so this thread does nothing
-//           between MMAs but one barrier wait and the scale copies.
+//           commits multicast to both CTAs.  Scale copies take tensor-pipe
+//           time, so they are issued once per stage; the MMAs of K block j
+//           select byte j of the words through their scale ids.
 //   warps 4-7 epilogue of the CTA's own 128 rows
 //
 // Fused gate/up epilogue (kSwiglu): for the first MoE GEMM, whose B holds the

@@ -38,3 +38,19 @@ def test_single_cta_fallback_one_tile_past_the_limit(gg):
     p = synth.make_problem("contiguous", 64, 256, 256, sizes, seed=612, device=DEV)
     assert p.rows == PAIR_MAX_ROWS + 128
     print(_check(p, 2))
+
+
+def test_mxfp4_at_its_tile_limit(gg):
+    # the MXFP4 pair list holds 3968 row tiles (larger scale staging): 62 x 8192 rows
+    p = synth.make_problem("contiguous", 62, 256, 256, [8192] * 62, seed=613, device=DEV,
+                           scale_kind="mxfp4")
+    assert p.rows == 3968 * 128
+    print(_check(p, 3))
+
+
+def test_fp32_scales_at_the_tile_limit(gg):
+    # the promotion kernel shares the pair list (4096 row tiles)
+    p = synth.make_problem("contiguous", 64, 256, 256, [8192] * 64, seed=614, device=DEV,
+                           scale_kind="fp32")
+    assert p.rows == PAIR_MAX_ROWS
+    print(_check(p, 4))

@@ -194,3 +194,11 @@ def test_named_fused_workload_sampled_rows(gg, name):
     valid, untouched = synth.sample_rows(p, per_group=16, seed=2)
     stats = check_fused(p, q, s, valid, untouched)
     print(name, stats)
+
+
+def test_at_the_pair_list_limit(gg):
+    """4096 row tiles of 128 (m_sum = 524288), the most the pair list holds; sampled rows."""
+    p = synth.make_problem("contiguous", 64, 256, 256, [8192] * 64, seed=307, device=DEV)
+    q, s = run_fused(p, SA_MK)
+    valid, untouched = synth.sample_rows(p, per_group=8, seed=5)
+    print(check_fused(p, q, s, valid, untouched))

@@ -390,6 +390,27 @@ __device__ __forceinline__ PairUnit unit_of(const GemmParams& p, const int* list
     return w;
 }
 
+// L2 prefetch of a contiguous problem: the pairs working on one band share its A
+// tiles (one per column tile) and its B tiles (one per row tile).  The same boxes
+// prefetched by all of them flooded the L2 with duplicate misses, so only one
+// unit prefetches each: for A the unit with column tile 0, for B the unit with
+// the first row tile of its band -- in both cases the earliest of the sharers.
+// Masked problems keep every unit prefetching: restricting them the same way
+// (column tile 0 / a group's first row pair) made the masked workload 12% slower.
+template <bool kMasked>
+__device__ __forceinline__ bool prefetch_owner_of(const GemmParams& p, int total_units, int u,
+                                                  bool is_a) {
+    if constexpr (kMasked) {
+        return true;
+    } else {
+        const int band_units = 4 * p.num_n_tiles;
+        const int band = u / band_units;
+        const int r = u - band * band_units;
+        const int gp = min(4, total_units / p.num_n_tiles - band * 4);
+        return is_a ? r < gp : r % gp == 0;
+    }
+}
+
 template <typename OutT, bool kMasked, bool kSwiglu, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -516,6 +537,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         return pc;
     };
 
+    auto prefetch_owner = [&](int uu) {
+        return prefetch_owner_of<kMasked>(p, total_units, uu, warp == 0);
+    };
+
     // First A / B row of this CTA for unit u.
     auto unit_rows = [&](const PairUnit& w, int64_t* a_row0, int* b_row0) {
         *a_row0 = kMasked ? static_cast<int64_t>(w.g) * p.rows + w.m_base
@@ -561,10 +586,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     // (the next piece's first steps near the end of this one)
                     int kp = ks + L::kPrefetchStages;
                     int32_t prow = row0;
-                    bool pf = true;
+                    bool pf = prefetch_owner(pc.u);
                     if (kp >= pc.ks1) {
                         const PairPiece np = get_piece(pi + 1);
-                        pf = np.u >= 0;
+                        pf = np.u >= 0 && prefetch_owner(np.u);
                         if (pf) {
                             int64_t na;
                             int nbr;

@@ -143,6 +143,7 @@ grouped_gemm_promote_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 is_a ? static_cast<int32_t>(kMasked ? static_cast<int64_t>(w.g) * p.rows + w.m_base
                                                     : static_cast<int64_t>(w.m_base))
                      : w.g * p.n + w.n_tile * 256 + static_cast<int>(rank) * 128;
+            const bool pf_owner = prefetch_owner_of<kMasked>(p, total_units, u, is_a);
             for (int ks = 0; ks < NKS; ++ks) {
                 if (!pair_warp_wait(bar_empty(s), ph ^ 1u, abort_flag, peer_abort, p.err)) {
                     aborted = true;
@@ -152,8 +153,9 @@ grouped_gemm_promote_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     if (leader) mbar_arrive_expect_tx(bar_full(s), 2u * L::kAStageBytes);
                     tma_load_3d_pair(sbase + op_off + s * L::kAStageBytes, map, 0, row0,
                                      ks * L::kKbPerStage, mapa_shared(bar_full(s), 0));
-                    // warm L2 with the box of this unit kPrefetchStages steps later
-                    if (ks + L::kPrefetchStages < NKS)
+                    // warm L2 with the box of this unit kPrefetchStages steps later (one
+                    // prefetcher per shared tile, as in the pair kernel)
+                    if (pf_owner && ks + L::kPrefetchStages < NKS)
                         tma_prefetch_3d(map, 0, row0, (ks + L::kPrefetchStages) * L::kKbPerStage);
                 }
                 if (++s == S) { s = 0; ph ^= 1u; }

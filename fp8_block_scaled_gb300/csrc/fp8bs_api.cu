@@ -99,6 +99,50 @@ SkWorkspace* sk_workspace(int dev, cudaStream_t stream, int slots) {
     return &(g_sk[key] = w);
 }
 
+// Device pair list of a contiguous problem whose row tiles outnumber the kernel's
+// shared-memory list: one region of `stride` ints per CTA of a grid of at most `ctas`
+// CTAs, kept per (device, stream) and grown on demand -- not while the stream is
+// capturing a graph (cudaMalloc is not captured), where the caller falls back or fails.
+struct ListWorkspace {
+    int* buf = nullptr;
+    int64_t ints = 0;
+};
+std::map<std::pair<int, void*>, ListWorkspace> g_list;
+
+struct PairList {
+    int* buf = nullptr;
+    int stride = 0;
+};
+
+bool pair_list_workspace(int dev, cudaStream_t stream, int ctas, int64_t m_tiles, PairList* out) {
+    const int64_t stride = (m_tiles + 1 + 31) / 32 * 32;
+    const int64_t ints = stride * ctas;
+    auto key = std::make_pair(dev, static_cast<void*>(stream));
+    auto it = g_list.find(key);
+    if (it == g_list.end() || it->second.ints < ints) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+            cudaGetLastError();
+            return false;
+        }
+        if (it != g_list.end()) {
+            cudaStreamSynchronize(stream);
+            cudaFree(it->second.buf);
+            g_list.erase(it);
+        }
+        ListWorkspace w;
+        if (cudaMalloc(&w.buf, sizeof(int) * ints) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        w.ints = ints;
+        it = g_list.emplace(key, w).first;
+    }
+    out->buf = it->second.buf;
+    out->stride = static_cast<int>(stride);
+    return true;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Resolve the current device and its cached state (lock held by caller).
@@ -544,8 +588,14 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     int dev = 0;
     cudaGetDevice(&dev);
     const int64_t m_tiles = (m_sum + 127) / 128;
-    const bool pair = n % 256 == 0 && aligned(d, 32) && m_tiles <= fp8bs::kPairMaxTiles &&
-                      num_groups < (1 << 18);
+    bool pair = n % 256 == 0 && aligned(d, 32) && m_tiles <= fp8bs::kPairMaxTilesWs &&
+                num_groups < fp8bs::kPairMaxGroups;
+    // a pair list longer than shared memory holds goes to a device workspace; without
+    // one (a first such call while capturing a graph) the single-CTA kernel runs
+    PairList plist;
+    if (pair && m_tiles > fp8bs::kPairMaxTiles &&
+        !pair_list_workspace(dev, static_cast<cudaStream_t>(stream), st->sms, m_tiles, &plist))
+        pair = false;
     const int bn = pair ? 256 : pick_bn(n);
     const CUtensorMap *ta = nullptr, *tb = nullptr;
     constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
@@ -575,6 +625,8 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     p.num_m_tiles = static_cast<int>((m_sum + 127) / 128);
     p.num_n_tiles = static_cast<int>(n / bn);
     p.raster_band = 8;
+    p.list_ws = plist.buf;
+    p.list_ws_stride = plist.stride;
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
     if (pair)
         return dispatch_pair<false>(*st, out_dtype, *ta, *tb, p, tiles,
@@ -681,7 +733,8 @@ int gemm_grouped_contiguous_silu_mul_quant(const void* a, const float* scale_a, 
     if (!grouped_layout || !aligned(grouped_layout, 4) || !aligned(out, 32))
         return FP8BS_ERR_INVALID_ARG;
     const int64_t m_tiles = (m_sum + 127) / 128;
-    if (m_tiles > fp8bs::kPairMaxTiles || num_groups >= (1 << 18)) return FP8BS_ERR_INVALID_ARG;
+    if (m_tiles > fp8bs::kPairMaxTilesWs || num_groups >= fp8bs::kPairMaxGroups)
+        return FP8BS_ERR_INVALID_ARG;
 
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState* st = nullptr;
@@ -689,6 +742,10 @@ int gemm_grouped_contiguous_silu_mul_quant(const void* a, const float* scale_a, 
     if (rc != FP8BS_OK) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
+    PairList plist;
+    if (m_tiles > fp8bs::kPairMaxTiles &&
+        !pair_list_workspace(dev, static_cast<cudaStream_t>(stream), st->sms, m_tiles, &plist))
+        return FP8BS_ERR_CUDA;  // a first call this large while the stream captures a graph
     const CUtensorMap *ta = nullptr, *tb = nullptr;
     constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
     if ((rc = get_map3(dev, a, k, m_sum, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
@@ -716,6 +773,8 @@ int gemm_grouped_contiguous_silu_mul_quant(const void* a, const float* scale_a, 
     p.qs_g_stride = 0;
     p.qs_row_stride = out_scale_layout == FP8BS_SA_KM ? 1 : n / 256;
     p.qs_col_stride = out_scale_layout == FP8BS_SA_KM ? ld_out_scale : 1;
+    p.list_ws = plist.buf;
+    p.list_ws_stride = plist.stride;
     return launch_pair<__nv_bfloat16, false, true>(*st, 24, *ta, *tb, p,
                                                    m_tiles * p.num_n_tiles,
                                                    static_cast<cudaStream_t>(stream));
@@ -799,7 +858,7 @@ int gemm_grouped_contiguous_fp32_scales(const void* a, const float* scale_a, int
     if (v != FP8BS_OK) return v;
     const int64_t m_tiles = (m_sum + 127) / 128;
     if (!grouped_layout || !aligned(grouped_layout, 4) || !aligned(d, 32) ||
-        m_tiles > fp8bs::kPairMaxTiles || num_groups >= (1 << 18))
+        m_tiles > fp8bs::kPairMaxTilesWs || num_groups >= fp8bs::kPairMaxGroups)
         return FP8BS_ERR_INVALID_ARG;
 
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -808,6 +867,10 @@ int gemm_grouped_contiguous_fp32_scales(const void* a, const float* scale_a, int
     if (rc != FP8BS_OK) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
+    PairList plist;
+    if (m_tiles > fp8bs::kPairMaxTiles &&
+        !pair_list_workspace(dev, static_cast<cudaStream_t>(stream), st->sms, m_tiles, &plist))
+        return FP8BS_ERR_CUDA;  // a first call this large while the stream captures a graph
     const CUtensorMap *ta = nullptr, *tb = nullptr;
     constexpr uint32_t kKbBox = fp8bs::PromoteLayout::kKbPerStage;
     if ((rc = get_map3(dev, a, k, m_sum, 128, kKbBox, &ta)) != FP8BS_OK) return rc;
@@ -831,6 +894,8 @@ int gemm_grouped_contiguous_fp32_scales(const void* a, const float* scale_a, int
     p.num_m_tiles = static_cast<int>(m_tiles);
     p.num_n_tiles = static_cast<int>(n / 256);
     p.raster_band = 8;
+    p.list_ws = plist.buf;
+    p.list_ws_stride = plist.stride;
     const int64_t units = m_tiles * p.num_n_tiles;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return out_dtype == FP8BS_OUT_BF16
@@ -922,8 +987,8 @@ int gemm_grouped_contiguous_mxfp4(const void* a, const uint8_t* scale_a, const v
     int v = validate_mx(a, scale_a, b, scale_b, d, out_dtype, n, k, num_groups);
     if (v != FP8BS_OK) return v;
     const int64_t m_tiles = (m_sum + 127) / 128;
-    if (!grouped_layout || !aligned(grouped_layout, 4) || m_tiles > fp8bs::kMxMaxTiles ||
-        num_groups >= (1 << 18))
+    if (!grouped_layout || !aligned(grouped_layout, 4) || m_tiles > fp8bs::kPairMaxTilesWs ||
+        num_groups >= fp8bs::kPairMaxGroups)
         return FP8BS_ERR_INVALID_ARG;
 
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -932,6 +997,10 @@ int gemm_grouped_contiguous_mxfp4(const void* a, const uint8_t* scale_a, const v
     if (rc != FP8BS_OK) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
+    PairList plist;
+    if (m_tiles > fp8bs::kMxMaxTiles &&
+        !pair_list_workspace(dev, static_cast<cudaStream_t>(stream), st->sms, m_tiles, &plist))
+        return FP8BS_ERR_CUDA;  // a first call this large while the stream captures a graph
     const CUtensorMap *ta = nullptr, *tb = nullptr;
     constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
     // packed rows: k/2 bytes, K blocks of 128 bytes
@@ -954,6 +1023,8 @@ int gemm_grouped_contiguous_mxfp4(const void* a, const uint8_t* scale_a, const v
     p.num_m_tiles = static_cast<int>(m_tiles);
     p.num_n_tiles = static_cast<int>(n / 256);
     p.raster_band = 8;
+    p.list_ws = plist.buf;
+    p.list_ws_stride = plist.stride;
     const int64_t tiles = m_tiles * p.num_n_tiles;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return out_dtype == FP8BS_OUT_BF16
@@ -1034,7 +1105,8 @@ int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_
     if (!grouped_layout || !aligned(grouped_layout, 4)) return FP8BS_ERR_INVALID_ARG;
     // only shapes the CTA-pair kernel takes
     const int64_t m_tiles = (m_sum + 127) / 128;
-    if (n % 256 != 0 || !aligned(d, 32) || m_tiles > fp8bs::kPairMaxTiles || num_groups >= (1 << 18))
+    if (n % 256 != 0 || !aligned(d, 32) || m_tiles > fp8bs::kPairMaxTiles ||
+        num_groups >= fp8bs::kPairMaxGroups)
         return FP8BS_ERR_INVALID_ARG;
 
     std::lock_guard<std::mutex> lock(g_mutex);

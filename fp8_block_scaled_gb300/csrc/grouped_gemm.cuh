@@ -77,6 +77,9 @@ struct GemmParams {
     int64_t qs_row_stride;       // elements between rows
     int64_t qs_col_stride;       // elements between 128-column blocks
     uint32_t debug_flags;        // kDebug* test hooks, 0 in normal use
+    int* list_ws;                // pair kernels: device pair list (list_ws_stride ints per
+                                 // CTA) when it outgrows shared memory, else null
+    int list_ws_stride;
 };
 
 template <int BN>

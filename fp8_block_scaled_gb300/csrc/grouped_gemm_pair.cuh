@@ -70,7 +70,12 @@
 
 namespace fp8bs {
 
-constexpr int kPairMaxTiles = 4096;  // contiguous: max 128-row tiles (m_sum <= 524288)
+constexpr int kPairMaxTiles = 4096;  // contiguous: 128-row tiles the shared-memory list holds
+// contiguous, with the pair list in a device workspace: the prologue's layout
+// scan indexes the operand stages as 4-byte entries (192 KB), and an entry holds
+// a 16-bit tile index
+constexpr int kPairMaxTilesWs = 32768;    // m_sum <= 4194304
+constexpr int kPairMaxGroups = 1 << 15;   // expert ids of a pair-list entry
 constexpr int kMxMaxTiles = 3968;    // MXFP4 (larger scale staging): m_sum <= 507904
 
 // Shared-memory plan of the CTA-pair kernel.  kMx selects the MXFP4 variant:
@@ -115,16 +120,19 @@ struct PairLayoutT {
     static_assert(kKbPerStage <= 4, "E4M3 scale words hold one byte per K block of a stage");
     static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
     static_assert(kPairMaxTiles * 4 <= kStages * kAStageBytes, "prologue scratch");
+    static_assert(kPairMaxTilesWs * 4 <= kStages * (kAStageBytes + kBStageBytes) &&
+                      kOffB == kOffA + kStages * kAStageBytes,
+                  "prologue scratch of a workspace-sized list (A and B stages contiguous)");
     static_assert(kPartChunks == 4 && kAStageBytes == kPartChunkBytes &&
                       kBStageBytes == kPartChunkBytes && kStages >= 2,
                   "stream-K partial staging: chunks fill the A and B halves of two stages");
 };
 using PairLayout = PairLayoutT<false>;
 
-// Contiguous pair-list entry: first 128-row tile (12 bits), "second tile not
-// part of the pair" flag (bit 12), expert id (bits 13..31).
+// Contiguous pair-list entry: first 128-row tile (bits 0..15), "second tile not
+// part of the pair" flag (bit 16), expert id (bits 17..31).
 __device__ __forceinline__ uint32_t pack_pair(int t0, bool half, int g) {
-    return static_cast<uint32_t>(t0) | (half ? 1u << 12 : 0u) | (static_cast<uint32_t>(g) << 13);
+    return static_cast<uint32_t>(t0) | (half ? 1u << 16 : 0u) | (static_cast<uint32_t>(g) << 17);
 }
 
 // SiLU with the hardware exponential and the approximate (reciprocal-based)
@@ -273,24 +281,27 @@ __device__ __forceinline__ int build_units(const GemmParams& p, uint8_t* scratch
         // ---- pair list: tiles of each expert segment, two by two
         const int T = p.num_m_tiles;
         int* E = reinterpret_cast<int*>(scratch_smem);
-        // all of this thread's grouped_layout reads are issued before the first is used
+        // all of a round's grouped_layout reads are issued before the first is used
+        // (one round covers a list that fits shared memory)
         constexpr int kLoads = (kPairMaxTiles + NT - 1) / NT;
-        int ev[kLoads];
+        for (int base = 0; base < T; base += kLoads * NT) {
+            int ev[kLoads];
 #pragma unroll
-        for (int j = 0; j < kLoads; ++j) {
-            const int t = static_cast<int>(threadIdx.x) + j * NT;
-            ev[j] = t < T ? __ldg(p.row_info + static_cast<int64_t>(t) * kBM) : -1;
-        }
+            for (int j = 0; j < kLoads; ++j) {
+                const int t = base + static_cast<int>(threadIdx.x) + j * NT;
+                ev[j] = t < T ? __ldg(p.row_info + static_cast<int64_t>(t) * kBM) : -1;
+            }
 #pragma unroll
-        for (int j = 0; j < kLoads; ++j) {
-            const int t = static_cast<int>(threadIdx.x) + j * NT;
-            if (t < T) {
-                int v = ev[j];
-                if (v >= p.num_groups || v < -1) {
-                    raise_error(p.err, kErrBadGroup);
-                    v = -1;
+            for (int j = 0; j < kLoads; ++j) {
+                const int t = base + static_cast<int>(threadIdx.x) + j * NT;
+                if (t < T) {
+                    int v = ev[j];
+                    if (v >= p.num_groups || v < -1) {
+                        raise_error(p.err, kErrBadGroup);
+                        v = -1;
+                    }
+                    E[t] = v;
                 }
-                E[t] = v;
             }
         }
         __syncthreads();
@@ -369,9 +380,9 @@ __device__ __forceinline__ PairUnit unit_of(const GemmParams& p, const int* list
         const int pi = band * 4 + r % gp;
         w.n_tile = r / gp;
         const uint32_t e = static_cast<uint32_t>(list[pi]);
-        const int t0 = static_cast<int>(e & 0xFFFu);
-        const bool half = (e >> 12) & 1u;
-        w.g = static_cast<int>(e >> 13);
+        const int t0 = static_cast<int>(e & 0xFFFFu);
+        const bool half = (e >> 16) & 1u;
+        w.g = static_cast<int>(e >> 17);
         w.m_base = (t0 + static_cast<int>(rank)) * kBM;
         w.store = !(half && rank == 1);
     } else {
@@ -438,7 +449,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
     int* scan_scratch = reinterpret_cast<int*>(smem + L::kOffMisc + 16);
-    int* list = reinterpret_cast<int*>(smem + L::kOffList);
+    // the pair list: in shared memory, or this CTA's region of the device workspace
+    int* list = p.list_ws != nullptr
+                    ? p.list_ws + static_cast<int64_t>(blockIdx.x) * p.list_ws_stride
+                    : reinterpret_cast<int*>(smem + L::kOffList);
     const uint32_t peer_abort = mapa_shared(smem_addr(smem + L::kOffMisc + 4), rank ^ 1u);
 
     // ---------------------------------------------------------------- setup

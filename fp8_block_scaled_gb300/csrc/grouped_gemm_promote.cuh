@@ -54,6 +54,9 @@ struct PromoteLayout {
     static constexpr int kTmemCols = 512;                     // two 256-column partial buffers
     static_assert(kBytes + kAlignSlack <= 232448, "shared memory budget");
     static_assert(kPairMaxTiles * 4 <= kStages * kAStageBytes, "prologue scratch");
+    static_assert(kPairMaxTilesWs * 4 <= kStages * (kAStageBytes + kBStageBytes) &&
+                      kOffB == kOffA + kStages * kAStageBytes,
+                  "prologue scratch of a workspace-sized list (A and B stages contiguous)");
 };
 
 // tcgen05 instruction descriptor, kind::f8f6f4: fp32 accumulator (bits 4-5 = 1),
@@ -88,7 +91,9 @@ grouped_gemm_promote_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
     int* scan_scratch = reinterpret_cast<int*>(smem + L::kOffMisc + 16);
-    int* list = reinterpret_cast<int*>(smem + L::kOffList);
+    int* list = p.list_ws != nullptr
+                    ? p.list_ws + static_cast<int64_t>(blockIdx.x) * p.list_ws_stride
+                    : reinterpret_cast<int*>(smem + L::kOffList);
     const uint32_t peer_abort = mapa_shared(smem_addr(smem + L::kOffMisc + 4), rank ^ 1u);
 
     // ---------------------------------------------------------------- setup

@@ -44,7 +44,13 @@
  *    a capture on a stream that has already run one call replays to the same
  *    bits as the eager call.  Launches on one stream share the
  *    workspace safely; concurrent launches on different streams use
- *    different workspaces.
+ *    different workspaces.  The contiguous variants keep their list of
+ *    expert tile pairs in shared memory up to 524288 rows (507904 for MXFP4)
+ *    and above that in a second per-stream workspace (about 4 bytes per
+ *    128-row tile per SM, up to 4194304 rows), allocated the same way; when
+ *    it cannot be had, gemm_grouped_contiguous runs the one-CTA kernel
+ *    instead (same results) and the other contiguous entry points return
+ *    FP8BS_ERR_CUDA.
  *  - Rows that are not computed (grouped_layout == -1, or m >= masked_m[g])
  *    are not written: D keeps its prior contents there.
  *  - Return value: FP8BS_OK, or an error code; nothing is enqueued on error.
@@ -157,9 +163,12 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
  *              ld_out_scale % 4 == 0, 16-byte aligned.  Either is a scale_a
  *              layout of gemm_grouped_contiguous, so (out, out_scale) is the
  *              activation operand of the down projection as it stands.
- *   n % 256 == 0 (n/2 a multiple of 128), m_sum <= 524288, num_groups < 2^18:
+ *   n % 256 == 0 (n/2 a multiple of 128), m_sum <= 4194304, num_groups < 2^15:
  *              the op runs on the CTA-pair kernel only; other shapes return
- *              FP8BS_ERR_INVALID_ARG.
+ *              FP8BS_ERR_INVALID_ARG.  Above 524288 rows the pair list lives in
+ *              a per-stream device workspace (grown on first use, like the
+ *              stream-K scratch): a call that would need to grow it while the
+ *              stream is being captured returns FP8BS_ERR_CUDA.
  * Rows with grouped_layout == -1 are written neither in out nor in out_scale.
  * Scratch as for gemm_grouped_contiguous (the per-stream stream-K workspace).
  */
@@ -202,8 +211,11 @@ int gemm_grouped_masked_silu_mul_quant(const void* a, const float* scale_a, int 
  * the hardware-scaled path on power-of-two scales.
  *
  * Runs on the CTA-pair kernel only: n % 256 == 0, d 32-byte aligned, and for
- * the contiguous variant m_sum <= 524288 rows and num_groups < 2^18; other
- * shapes return FP8BS_ERR_INVALID_ARG.  No scratch memory, no stream-K tail.
+ * the contiguous variant m_sum <= 4194304 rows and num_groups < 2^15; other
+ * shapes return FP8BS_ERR_INVALID_ARG.  No stream-K tail.  Above 524288 rows
+ * the pair list lives in the per-stream device workspace, as for
+ * gemm_grouped_contiguous_silu_mul_quant (FP8BS_ERR_CUDA when it would have
+ * to grow during stream capture); below that no scratch memory is used.
  */
 int gemm_grouped_contiguous_fp32_scales(const void* a, const float* scale_a, int sa_layout,
                                         int64_t ld_sa, const void* b, const float* scale_b,
@@ -233,8 +245,10 @@ int gemm_grouped_masked_fp32_scales(const void* a, const float* scale_a, int sa_
  *   scale_b  E8M0 bytes [num_groups, n, k/32] (one per row of B and 32-element
  *            block), 4-byte aligned
  *   d        out_dtype [m_sum, n] or [num_groups, m_max, n], 32-byte aligned
- *   n % 256 == 0, k % 256 == 0; contiguous: m_sum <= 507904 rows, num_groups
- *   < 2^18.  grouped_layout / masked_m / expected_m as for the E4M3 variants.
+ *   n % 256 == 0, k % 256 == 0; contiguous: m_sum <= 4194304 rows, num_groups
+ *   < 2^15 (above 507904 rows the pair list lives in the per-stream device
+ *   workspace, FP8BS_ERR_CUDA if it would have to grow during stream capture).
+ *   grouped_layout / masked_m / expected_m as for the E4M3 variants.
  * Runs on the CTA-pair kernel (with the stream-K tail for the contiguous
  * variant).
  */
@@ -272,7 +286,7 @@ int gemm_grouped_masked_mxfp4(const void* a, const uint8_t* scale_a, const void*
  *    TMA tensor maps are encoded on the stack for every call.
  * Returns FP8BS_ERR_INVALID_ARG, in addition to the cases of
  * gemm_grouped_contiguous, for shapes the CTA-pair kernel does not take
- * (n % 256 != 0, d not 32-byte aligned, m_sum > 524288 rows, num_groups >= 2^18)
+ * (n % 256 != 0, d not 32-byte aligned, m_sum > 524288 rows, num_groups >= 2^15)
  * and when the device would run more than 80 CTA pairs (more scratch than the
  * array holds).
  */

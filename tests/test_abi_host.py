@@ -131,8 +131,8 @@ def _noalloc(**kw):
 @pytest.mark.parametrize("bad", [
     dict(n=384),                 # the CTA-pair kernel needs N % 256 == 0
     dict(d=P + 16),              # and a 32-byte aligned D
-    dict(m_sum=524288 + 128),    # and at most 4096 row tiles
-    dict(g=1 << 18),             # and fewer than 2^18 groups
+    dict(m_sum=524288 + 128),    # and at most 4096 row tiles (no workspace for a longer list)
+    dict(g=1 << 15),             # and fewer than 2^15 groups (15-bit expert id of a list entry)
     dict(a=0), dict(k=100), dict(out=5),
 ])
 def test_noalloc_rejects(lib, bad):
@@ -170,8 +170,8 @@ def _fused_masked(**kw):
     dict(out=P + 16),            # codes are stored 32 bytes at a time
     dict(os=0), dict(os=P + 2), dict(osl=2),
     dict(osl=1, ldo=255), dict(osl=1, ldo=258), dict(osl=1, ldo=256, os=P + 4),
-    dict(m_sum=524288 + 128),    # pair-list limit
-    dict(g=1 << 18),
+    dict(m_sum=4194304 + 128),   # pair-list limit with the list in a device workspace
+    dict(g=1 << 15),
     dict(a=0), dict(lay=0), dict(k=100), dict(sa_layout=5),
 ])
 def test_fused_contiguous_rejects(lib, bad):
@@ -204,7 +204,7 @@ def _fp32s(**kw):
 @pytest.mark.parametrize("bad", [
     dict(n=384),                 # the promotion kernel is a CTA-pair kernel: n % 256 == 0
     dict(d=P + 16),              # 32-byte output stores
-    dict(m_sum=524288 + 128), dict(g=1 << 18),
+    dict(m_sum=4194304 + 128), dict(g=1 << 15),
     dict(a=0), dict(sa=0), dict(lay=0), dict(k=100), dict(out=2), dict(sa_layout=1, ld_sa=255),
 ])
 def test_fp32_scales_rejects(lib, bad):
@@ -238,7 +238,8 @@ def _mx(**kw):
     dict(k=128),                 # K blocks of 128 packed bytes: k % 256 == 0
     dict(n=384), dict(d=P + 16), dict(a=P + 8), dict(sa=P + 2), dict(sb=P + 1),
     dict(a=0), dict(sa=0), dict(lay=0), dict(out=3), dict(g=0),
-    dict(m_sum=507904 + 128),    # MX pair-list limit
+    dict(m_sum=4194304 + 128),   # pair-list limit with the list in a device workspace
+    dict(g=1 << 15),
 ])
 def test_mxfp4_rejects(lib, bad):
     assert _mx(**bad) == INVALID

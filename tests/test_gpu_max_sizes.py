@@ -1,9 +1,9 @@
-"""GPU parity at the contiguous pair path's size limit and just past it.
+"""GPU parity at the contiguous pair kernels' list limits and past them.
 
-The CTA-pair kernel keeps its list of expert tile pairs in shared memory, at
-most 4096 tiles of 128 rows (m_sum <= 524288).  A problem of exactly that many
-tiles must run on it; one tile more must fall back to the single-CTA kernel,
-which has no such list.  Both are checked against the oracle on seeded
+The CTA-pair kernels keep their list of expert tile pairs in shared memory for
+up to 4096 row tiles of 128 (3968 for MXFP4), and in a per-stream device
+workspace above that (up to 32768 tiles).  Problems at the shared-memory limit,
+one tile past it and far past it are checked against the oracle on seeded
 samples of rows (group edges + random rows) and on the untouched padding rows.
 """
 import pytest
@@ -32,7 +32,7 @@ def test_pair_path_at_the_tile_limit(gg):
     print(_check(p, 1))
 
 
-def test_single_cta_fallback_one_tile_past_the_limit(gg):
+def test_pair_list_in_workspace_one_tile_past_the_limit(gg):
     # one expert one row longer: 4097 row tiles, the last expert ragged
     sizes = [8192] * 63 + [8193]
     p = synth.make_problem("contiguous", 64, 256, 256, sizes, seed=612, device=DEV)
@@ -54,3 +54,19 @@ def test_fp32_scales_at_the_tile_limit(gg):
                            scale_kind="fp32")
     assert p.rows == PAIR_MAX_ROWS
     print(_check(p, 4))
+
+
+def test_workspace_list_a_million_rows(gg):
+    # 8192 row tiles: the pair list in the workspace, grouped_layout read in two rounds
+    p = synth.make_problem("contiguous", 128, 256, 256, [8192] * 128, seed=616, device=DEV)
+    assert p.rows == 2 * PAIR_MAX_ROWS
+    print(_check(p, 5))
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "fp32"])
+def test_variant_paths_past_the_shared_memory_list(gg, kind):
+    sizes = [8192] * 63 + [8193] if kind == "fp32" else [8192] * 62 + [1]
+    p = synth.make_problem("contiguous", len(sizes), 256, 256, sizes, seed=617, device=DEV,
+                           scale_kind=kind)
+    assert p.rows == (PAIR_MAX_ROWS if kind == "fp32" else 3968 * 128) + 128
+    print(_check(p, 6))

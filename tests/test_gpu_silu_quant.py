@@ -202,3 +202,11 @@ def test_at_the_pair_list_limit(gg):
     q, s = run_fused(p, SA_MK)
     valid, untouched = synth.sample_rows(p, per_group=8, seed=5)
     print(check_fused(p, q, s, valid, untouched))
+
+
+def test_past_the_shared_memory_pair_list(gg):
+    """4097 row tiles: the pair list goes to the device workspace; sampled rows."""
+    p = synth.make_problem("contiguous", 64, 256, 256, [8192] * 63 + [8193], seed=308, device=DEV)
+    q, s = run_fused(p, SA_MK)
+    valid, untouched = synth.sample_rows(p, per_group=8, seed=6)
+    print(check_fused(p, q, s, valid, untouched))

@@ -91,9 +91,13 @@ grouped_gemm_promote_kernel(const __grid_constant__ CUtensorMap tmap_a,
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
     int* scan_scratch = reinterpret_cast<int*>(smem + L::kOffMisc + 16);
-    int* list = p.list_ws != nullptr
-                    ? p.list_ws + static_cast<int64_t>(blockIdx.x) * p.list_ws_stride
-                    : reinterpret_cast<int*>(smem + L::kOffList);
+    // The pair list's address is formed again at every use instead of being held
+    // in a register for the whole kernel: a live 64-bit pointer here made the
+    // promotion warps spill.
+    auto list = [&]() {
+        if (p.list_ws == nullptr) return reinterpret_cast<int*>(smem + L::kOffList);
+        return p.list_ws + static_cast<int64_t>(cta_index_x()) * p.list_ws_stride;
+    };
     const uint32_t peer_abort = mapa_shared(smem_addr(smem + L::kOffMisc + 4), rank ^ 1u);
 
     // ---------------------------------------------------------------- setup
@@ -122,13 +126,13 @@ grouped_gemm_promote_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tmem_relinquish_pair();
     }
     const int total_units =
-        build_units<kMasked, kPromoteThreads>(p, smem + L::kOffA, list, scan_scratch);
+        build_units<kMasked, kPromoteThreads>(p, smem + L::kOffA, list(), scan_scratch);
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // peer barriers initialised, tensor memory allocated in both CTAs
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    auto get_unit = [&](int u) { return unit_of<kMasked>(p, list, total_units, u, rank); };
+    auto get_unit = [&](int u) { return unit_of<kMasked>(p, list(), total_units, u, rank); };
 
     constexpr uint32_t kIdesc = make_idesc_f8(2 * kBM, 256);
     const int KB = p.kb_count;

@@ -257,6 +257,14 @@ __device__ __forceinline__ void tc_ld_32x32b_x64_sync(uint32_t taddr, uint32_t (
 }
 
 // ------------------------------------------------------------------ CTA pairs (clusters of 2)
+// %ctaid.x read with a volatile move, so that a value derived from it is computed
+// again where it is used rather than kept live across the kernel.
+__device__ __forceinline__ uint32_t cta_index_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(r));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));

@@ -135,6 +135,14 @@ def _fp8_ptr(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
+def _contig_ptr(t: torch.Tensor, name: str) -> int:
+    # no silent .contiguous() copy: a temporary could be freed and its memory
+    # reused on torch's current stream while the kernel still reads it on another
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
 def _sa_layout_2d(sa: torch.Tensor, rows: int, kb: int):
     """(layout, ld) of a logical [rows, K/128] scale tensor from its strides."""
     if sa.dtype != torch.float32 or sa.shape != (rows, kb):
@@ -246,7 +254,7 @@ def gemm_grouped_contiguous(a, scale_a, b, scale_b, d, grouped_layout, *, stream
     layout, ld = _sa_layout_2d(scale_a, m_sum, k // 128)
     raw = _raw or gemm_grouped_contiguous_raw
     st = raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
-             scale_b.contiguous().data_ptr(), grouped_layout.contiguous().data_ptr(), d.data_ptr(),
+             _contig_ptr(scale_b, "scale_b"), _contig_ptr(grouped_layout, "grouped_layout"), d.data_ptr(),
              _out_code(d), m_sum, n, k, G, stream)
     _check(st, raw.__name__[:-4])
     return d
@@ -275,7 +283,7 @@ def gemm_grouped_masked(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0
     layout, ld = _sa_layout_3d(scale_a, G, m_max, k // 128)
     raw = _raw or gemm_grouped_masked_raw
     st = raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
-             scale_b.contiguous().data_ptr(), masked_m.contiguous().data_ptr(), expected_m,
+             _contig_ptr(scale_b, "scale_b"), _contig_ptr(masked_m, "masked_m"), expected_m,
              d.data_ptr(), _out_code(d), G, m_max, n, k, stream)
     _check(st, raw.__name__[:-4])
     return d
@@ -336,7 +344,7 @@ def gemm_grouped_contiguous_silu_mul_quant(a, scale_a, b, scale_b, out, out_scal
     olayout, old = _sa_layout_2d(out_scale, m_sum, n // 256)
     st = gemm_grouped_contiguous_silu_mul_quant_raw(
         _fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
-        scale_b.contiguous().data_ptr(), grouped_layout.contiguous().data_ptr(), out.data_ptr(),
+        _contig_ptr(scale_b, "scale_b"), _contig_ptr(grouped_layout, "grouped_layout"), out.data_ptr(),
         out_scale.data_ptr(), olayout, old, m_sum, n, k, G, stream)
     _check(st, "gemm_grouped_contiguous_silu_mul_quant")
     return out, out_scale
@@ -360,7 +368,7 @@ def gemm_grouped_masked_silu_mul_quant(a, scale_a, b, scale_b, out, out_scale, m
     olayout, old = _sa_layout_3d(out_scale, G, m_max, n // 256)
     st = gemm_grouped_masked_silu_mul_quant_raw(
         _fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
-        scale_b.contiguous().data_ptr(), masked_m.contiguous().data_ptr(), expected_m,
+        _contig_ptr(scale_b, "scale_b"), _contig_ptr(masked_m, "masked_m"), expected_m,
         out.data_ptr(), out_scale.data_ptr(), olayout, old, G, m_max, n, k, stream)
     _check(st, "gemm_grouped_masked_silu_mul_quant")
     return out, out_scale
@@ -407,7 +415,7 @@ def gemm_grouped_contiguous_mxfp4(a, scale_a, b, scale_b, d, grouped_layout, *, 
         raise ValueError("grouped_layout must be int32")
     st = gemm_grouped_contiguous_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
                                            _u8(scale_b, "scale_b"),
-                                           grouped_layout.contiguous().data_ptr(), d.data_ptr(),
+                                           _contig_ptr(grouped_layout, "grouped_layout"), d.data_ptr(),
                                            _out_code(d), m_sum, n, k, G, stream)
     _check(st, "gemm_grouped_contiguous_mxfp4")
     return d
@@ -427,7 +435,7 @@ def gemm_grouped_masked_mxfp4(a, scale_a, b, scale_b, d, masked_m, expected_m: i
     if masked_m.dtype != torch.int32:
         raise ValueError("masked_m must be int32")
     st = gemm_grouped_masked_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
-                                       _u8(scale_b, "scale_b"), masked_m.contiguous().data_ptr(),
+                                       _u8(scale_b, "scale_b"), _contig_ptr(masked_m, "masked_m"),
                                        expected_m, d.data_ptr(), _out_code(d), G, m_max, n, k,
                                        stream)
     _check(st, "gemm_grouped_masked_mxfp4")

@@ -555,6 +555,13 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         return prefetch_owner_of<kMasked>(p, total_units, uu, warp == 0);
     };
 
+    // Masked: whether the 128 rows of group g starting at m0 hold a computed row.
+    auto half_has_rows = [&](int g, int m0) {
+        int mm = __ldg(p.row_info + g);
+        mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
+        return m0 < mm;
+    };
+
     // First A / B row of this CTA for unit u.
     auto unit_rows = [&](const PairUnit& w, int64_t* a_row0, int* b_row0) {
         *a_row0 = kMasked ? static_cast<int64_t>(w.g) * p.rows + w.m_base
@@ -583,6 +590,14 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const int32_t row0 = is_a ? static_cast<int32_t>(a_row0) : b_row0;
             const int64_t sa_goff = kMasked ? static_cast<int64_t>(w.g) * p.sa_g_stride : 0;
             const int nb0 = w.n_tile * 2;
+            // Masked: when the peer's 128 rows all lie at or past masked_m[g] (the last
+            // pair of a group with masked_m % 256 in [1, 128]), the peer loads no A and the
+            // leader arms for one CTA's A bytes.  The peer's stale A rows then enter the
+            // MMA, but row r of the product depends only on row r of A, and those rows are
+            // never stored.  Fewer L2 requests: about 2% on the masked decode workload.
+            const bool peer_a_skip =
+                kMasked && !kMx && !half_has_rows(w.g, w.m_base + (leader ? kBM : 0));
+            const bool own_a_skip = is_a && !leader && peer_a_skip;
             for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
                 if (!pair_warp_wait(bar_empty(s), ph ^ 1u, abort_flag, peer_abort, p.err)) {
                     aborted = true;
@@ -593,24 +608,29 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const uint32_t full_leader = mapa_shared(bar_full(s), 0);
                     // the leader arms its barrier for this operand's bytes of both CTAs; the
                     // peer's copies only complete into it
-                    if (leader) mbar_arrive_expect_tx(bar_full(s), 2u * L::kAStageBytes);
-                    tma_load_3d_pair(sbase + op_off + s * L::kAStageBytes, map, 0, row0, kb0,
-                                     full_leader);
+                    if (leader)
+                        mbar_arrive_expect_tx(bar_full(s),
+                                              (is_a && peer_a_skip ? 1u : 2u) * L::kAStageBytes);
+                    if (!own_a_skip)
+                        tma_load_3d_pair(sbase + op_off + s * L::kAStageBytes, map, 0, row0, kb0,
+                                         full_leader);
                     // warm L2 with the box this warp loads kPrefetchStages steps later
                     // (the next piece's first steps near the end of this one)
                     int kp = ks + L::kPrefetchStages;
                     int32_t prow = row0;
-                    bool pf = prefetch_owner(pc.u);
+                    bool pf = !own_a_skip && prefetch_owner(pc.u);
                     if (kp >= pc.ks1) {
                         const PairPiece np = get_piece(pi + 1);
                         pf = np.u >= 0 && prefetch_owner(np.u);
                         if (pf) {
                             int64_t na;
                             int nbr;
-                            unit_rows(get_unit(np.u), &na, &nbr);
+                            const PairUnit wn = get_unit(np.u);
+                            unit_rows(wn, &na, &nbr);
                             prow = is_a ? static_cast<int32_t>(na) : nbr;
                             kp = np.ks0 + (kp - pc.ks1);
-                            pf = kp < np.ks1;
+                            pf = kp < np.ks1 &&
+                                 !(is_a && kMasked && !kMx && !half_has_rows(wn.g, wn.m_base));
                         }
                     }
                     if (pf) tma_prefetch_3d(map, 0, prow, kp * L::kKbPerStage);

@@ -143,6 +143,21 @@ def _contig_ptr(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
+def _device_of(*tensors) -> torch.device:
+    """The one CUDA device holding every tensor.  The library launches on the
+    calling thread's current device, so a call with tensors of another device
+    (or of the host) would hand the kernel addresses it cannot use."""
+    dev = None
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"all tensors must be on one device ({dev} and {t.device} given)")
+    return dev
+
+
 def _sa_layout_2d(sa: torch.Tensor, rows: int, kb: int):
     """(layout, ld) of a logical [rows, K/128] scale tensor from its strides."""
     if sa.dtype != torch.float32 or sa.shape != (rows, kb):
@@ -248,14 +263,13 @@ def gemm_grouped_contiguous(a, scale_a, b, scale_b, d, grouped_layout, *, stream
         raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
     if grouped_layout.dtype != torch.int32 or not d.is_contiguous():
         raise ValueError("grouped_layout must be int32, d contiguous")
-    for t in (a, scale_a, b, scale_b, d, grouped_layout):
-        if not t.is_cuda:
-            raise ValueError("all tensors must be CUDA tensors")
+    dev = _device_of(a, scale_a, b, scale_b, d, grouped_layout)
     layout, ld = _sa_layout_2d(scale_a, m_sum, k // 128)
     raw = _raw or gemm_grouped_contiguous_raw
-    st = raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
-             _contig_ptr(scale_b, "scale_b"), _contig_ptr(grouped_layout, "grouped_layout"), d.data_ptr(),
-             _out_code(d), m_sum, n, k, G, stream)
+    with torch.cuda.device(dev):
+        st = raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
+                 _contig_ptr(scale_b, "scale_b"), _contig_ptr(grouped_layout, "grouped_layout"),
+                 d.data_ptr(), _out_code(d), m_sum, n, k, G, stream)
     _check(st, raw.__name__[:-4])
     return d
 
@@ -277,14 +291,13 @@ def gemm_grouped_masked(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0
         raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
     if masked_m.dtype != torch.int32 or not d.is_contiguous():
         raise ValueError("masked_m must be int32, d contiguous")
-    for t in (a, scale_a, b, scale_b, d, masked_m):
-        if not t.is_cuda:
-            raise ValueError("all tensors must be CUDA tensors")
+    dev = _device_of(a, scale_a, b, scale_b, d, masked_m)
     layout, ld = _sa_layout_3d(scale_a, G, m_max, k // 128)
     raw = _raw or gemm_grouped_masked_raw
-    st = raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
-             _contig_ptr(scale_b, "scale_b"), _contig_ptr(masked_m, "masked_m"), expected_m,
-             d.data_ptr(), _out_code(d), G, m_max, n, k, stream)
+    with torch.cuda.device(dev):
+        st = raw(_fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
+                 _contig_ptr(scale_b, "scale_b"), _contig_ptr(masked_m, "masked_m"), expected_m,
+                 d.data_ptr(), _out_code(d), G, m_max, n, k, stream)
     _check(st, raw.__name__[:-4])
     return d
 
@@ -337,15 +350,14 @@ def gemm_grouped_contiguous_silu_mul_quant(a, scale_a, b, scale_b, out, out_scal
     if scale_b.shape != (G, n // 128, k // 128) or scale_b.dtype != torch.float32:
         raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
     _check_out(out, out_scale, (m_sum,), n)
-    for t in (a, scale_a, b, scale_b, out, out_scale, grouped_layout):
-        if not t.is_cuda:
-            raise ValueError("all tensors must be CUDA tensors")
+    dev = _device_of(a, scale_a, b, scale_b, out, out_scale, grouped_layout)
     layout, ld = _sa_layout_2d(scale_a, m_sum, k // 128)
     olayout, old = _sa_layout_2d(out_scale, m_sum, n // 256)
-    st = gemm_grouped_contiguous_silu_mul_quant_raw(
-        _fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
-        _contig_ptr(scale_b, "scale_b"), _contig_ptr(grouped_layout, "grouped_layout"), out.data_ptr(),
-        out_scale.data_ptr(), olayout, old, m_sum, n, k, G, stream)
+    with torch.cuda.device(dev):
+        st = gemm_grouped_contiguous_silu_mul_quant_raw(
+            _fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
+            _contig_ptr(scale_b, "scale_b"), _contig_ptr(grouped_layout, "grouped_layout"),
+            out.data_ptr(), out_scale.data_ptr(), olayout, old, m_sum, n, k, G, stream)
     _check(st, "gemm_grouped_contiguous_silu_mul_quant")
     return out, out_scale
 
@@ -361,15 +373,14 @@ def gemm_grouped_masked_silu_mul_quant(a, scale_a, b, scale_b, out, out_scale, m
     if scale_b.shape != (G, n // 128, k // 128) or scale_b.dtype != torch.float32:
         raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
     _check_out(out, out_scale, (G, m_max), n)
-    for t in (a, scale_a, b, scale_b, out, out_scale, masked_m):
-        if not t.is_cuda:
-            raise ValueError("all tensors must be CUDA tensors")
+    dev = _device_of(a, scale_a, b, scale_b, out, out_scale, masked_m)
     layout, ld = _sa_layout_3d(scale_a, G, m_max, k // 128)
     olayout, old = _sa_layout_3d(out_scale, G, m_max, n // 256)
-    st = gemm_grouped_masked_silu_mul_quant_raw(
-        _fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
-        _contig_ptr(scale_b, "scale_b"), _contig_ptr(masked_m, "masked_m"), expected_m,
-        out.data_ptr(), out_scale.data_ptr(), olayout, old, G, m_max, n, k, stream)
+    with torch.cuda.device(dev):
+        st = gemm_grouped_masked_silu_mul_quant_raw(
+            _fp8_ptr(a, "a"), scale_a.data_ptr(), layout, ld, _fp8_ptr(b, "b"),
+            _contig_ptr(scale_b, "scale_b"), _contig_ptr(masked_m, "masked_m"), expected_m,
+            out.data_ptr(), out_scale.data_ptr(), olayout, old, G, m_max, n, k, stream)
     _check(st, "gemm_grouped_masked_silu_mul_quant")
     return out, out_scale
 
@@ -413,10 +424,12 @@ def gemm_grouped_contiguous_mxfp4(a, scale_a, b, scale_b, d, grouped_layout, *, 
         raise ValueError("d must be contiguous [M_sum, N], grouped_layout [M_sum]")
     if grouped_layout.dtype != torch.int32:
         raise ValueError("grouped_layout must be int32")
-    st = gemm_grouped_contiguous_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
-                                           _u8(scale_b, "scale_b"),
-                                           _contig_ptr(grouped_layout, "grouped_layout"), d.data_ptr(),
-                                           _out_code(d), m_sum, n, k, G, stream)
+    dev = _device_of(a, scale_a, b, scale_b, d, grouped_layout)
+    with torch.cuda.device(dev):
+        st = gemm_grouped_contiguous_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
+                                               _u8(scale_b, "scale_b"),
+                                               _contig_ptr(grouped_layout, "grouped_layout"),
+                                               d.data_ptr(), _out_code(d), m_sum, n, k, G, stream)
     _check(st, "gemm_grouped_contiguous_mxfp4")
     return d
 
@@ -434,10 +447,12 @@ def gemm_grouped_masked_mxfp4(a, scale_a, b, scale_b, d, masked_m, expected_m: i
         raise ValueError("d must be contiguous [G, M_max, N], masked_m [G]")
     if masked_m.dtype != torch.int32:
         raise ValueError("masked_m must be int32")
-    st = gemm_grouped_masked_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
-                                       _u8(scale_b, "scale_b"), _contig_ptr(masked_m, "masked_m"),
-                                       expected_m, d.data_ptr(), _out_code(d), G, m_max, n, k,
-                                       stream)
+    dev = _device_of(a, scale_a, b, scale_b, d, masked_m)
+    with torch.cuda.device(dev):
+        st = gemm_grouped_masked_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
+                                           _u8(scale_b, "scale_b"),
+                                           _contig_ptr(masked_m, "masked_m"), expected_m,
+                                           d.data_ptr(), _out_code(d), G, m_max, n, k, stream)
     _check(st, "gemm_grouped_masked_mxfp4")
     return d
 

@@ -119,6 +119,30 @@ def test_scale_layout_from_strides():
     assert _binding._sa_layout_3d(s3[:, :, :5].transpose(1, 2), 3, 5, KB) == (fb.SA_KM, 8)
 
 
+def test_wrappers_reject_host_tensors():
+    # checked in the binding before any library call: a host tensor would reach the
+    # kernel as an address it cannot use
+    a = torch.zeros(256, 256, dtype=torch.uint8)
+    sa = torch.ones(256, 2)
+    b = torch.zeros(2, 256, 256, dtype=torch.uint8)
+    sb = torch.ones(2, 2, 2)
+    d = torch.zeros(256, 256, dtype=torch.bfloat16)
+    lay = torch.zeros(256, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        fb.gemm_grouped_contiguous(a, sa, b, sb, d, lay)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        fb.gemm_grouped_masked(a.view(1, 256, 256), sa.view(1, 256, 2), b[:1], sb[:1],
+                               d.view(1, 256, 256), torch.zeros(1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        fb.gemm_grouped_contiguous_mxfp4(a[:, :128], torch.zeros(256, 8, dtype=torch.uint8),
+                                         b[:, :, :128], torch.zeros(2, 256, 8, dtype=torch.uint8),
+                                         d, lay)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        fb.gemm_grouped_contiguous_silu_mul_quant(a, sa, b, sb,
+                                                  torch.zeros(256, 128, dtype=torch.uint8),
+                                                  torch.ones(256, 1), lay)
+
+
 def _noalloc(**kw):
     args = dict(a=P, sa=P, sa_layout=0, ld_sa=0, b=P, sb=P, lay=P, d=P, out=0,
                 m_sum=256, n=256, k=256, g=2)

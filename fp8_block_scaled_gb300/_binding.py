@@ -143,10 +143,10 @@ def _contig_ptr(t: torch.Tensor, name: str) -> int:
     return t.data_ptr()
 
 
-def _device_of(*tensors) -> torch.device:
-    """The one CUDA device holding every tensor.  The library launches on the
-    calling thread's current device, so a call with tensors of another device
-    (or of the host) would hand the kernel addresses it cannot use."""
+def _device_of(*tensors, stream=None) -> torch.device:
+    """The one CUDA device holding every tensor (and the given torch stream).  The
+    library launches on the calling thread's current device, so a call with tensors
+    of another device (or of the host) would hand the kernel addresses it cannot use."""
     dev = None
     for t in tensors:
         if not t.is_cuda:
@@ -155,6 +155,9 @@ def _device_of(*tensors) -> torch.device:
             dev = t.device
         elif t.device != dev:
             raise ValueError(f"all tensors must be on one device ({dev} and {t.device} given)")
+    sdev = getattr(stream, "device", None)
+    if isinstance(sdev, torch.device) and sdev != dev:
+        raise ValueError(f"stream is on {sdev}, the tensors on {dev}")
     return dev
 
 
@@ -263,7 +266,7 @@ def gemm_grouped_contiguous(a, scale_a, b, scale_b, d, grouped_layout, *, stream
         raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
     if grouped_layout.dtype != torch.int32 or not d.is_contiguous():
         raise ValueError("grouped_layout must be int32, d contiguous")
-    dev = _device_of(a, scale_a, b, scale_b, d, grouped_layout)
+    dev = _device_of(a, scale_a, b, scale_b, d, grouped_layout, stream=stream)
     layout, ld = _sa_layout_2d(scale_a, m_sum, k // 128)
     raw = _raw or gemm_grouped_contiguous_raw
     with torch.cuda.device(dev):
@@ -291,7 +294,7 @@ def gemm_grouped_masked(a, scale_a, b, scale_b, d, masked_m, expected_m: int = 0
         raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
     if masked_m.dtype != torch.int32 or not d.is_contiguous():
         raise ValueError("masked_m must be int32, d contiguous")
-    dev = _device_of(a, scale_a, b, scale_b, d, masked_m)
+    dev = _device_of(a, scale_a, b, scale_b, d, masked_m, stream=stream)
     layout, ld = _sa_layout_3d(scale_a, G, m_max, k // 128)
     raw = _raw or gemm_grouped_masked_raw
     with torch.cuda.device(dev):
@@ -350,7 +353,7 @@ def gemm_grouped_contiguous_silu_mul_quant(a, scale_a, b, scale_b, out, out_scal
     if scale_b.shape != (G, n // 128, k // 128) or scale_b.dtype != torch.float32:
         raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
     _check_out(out, out_scale, (m_sum,), n)
-    dev = _device_of(a, scale_a, b, scale_b, out, out_scale, grouped_layout)
+    dev = _device_of(a, scale_a, b, scale_b, out, out_scale, grouped_layout, stream=stream)
     layout, ld = _sa_layout_2d(scale_a, m_sum, k // 128)
     olayout, old = _sa_layout_2d(out_scale, m_sum, n // 256)
     with torch.cuda.device(dev):
@@ -373,7 +376,7 @@ def gemm_grouped_masked_silu_mul_quant(a, scale_a, b, scale_b, out, out_scale, m
     if scale_b.shape != (G, n // 128, k // 128) or scale_b.dtype != torch.float32:
         raise ValueError("scale_b must be fp32 [G, N/128, K/128]")
     _check_out(out, out_scale, (G, m_max), n)
-    dev = _device_of(a, scale_a, b, scale_b, out, out_scale, masked_m)
+    dev = _device_of(a, scale_a, b, scale_b, out, out_scale, masked_m, stream=stream)
     layout, ld = _sa_layout_3d(scale_a, G, m_max, k // 128)
     olayout, old = _sa_layout_3d(out_scale, G, m_max, n // 256)
     with torch.cuda.device(dev):
@@ -424,7 +427,7 @@ def gemm_grouped_contiguous_mxfp4(a, scale_a, b, scale_b, d, grouped_layout, *, 
         raise ValueError("d must be contiguous [M_sum, N], grouped_layout [M_sum]")
     if grouped_layout.dtype != torch.int32:
         raise ValueError("grouped_layout must be int32")
-    dev = _device_of(a, scale_a, b, scale_b, d, grouped_layout)
+    dev = _device_of(a, scale_a, b, scale_b, d, grouped_layout, stream=stream)
     with torch.cuda.device(dev):
         st = gemm_grouped_contiguous_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
                                                _u8(scale_b, "scale_b"),
@@ -447,7 +450,7 @@ def gemm_grouped_masked_mxfp4(a, scale_a, b, scale_b, d, masked_m, expected_m: i
         raise ValueError("d must be contiguous [G, M_max, N], masked_m [G]")
     if masked_m.dtype != torch.int32:
         raise ValueError("masked_m must be int32")
-    dev = _device_of(a, scale_a, b, scale_b, d, masked_m)
+    dev = _device_of(a, scale_a, b, scale_b, d, masked_m, stream=stream)
     with torch.cuda.device(dev):
         st = gemm_grouped_masked_mxfp4_raw(_u8(a, "a"), _u8(scale_a, "scale_a"), _u8(b, "b"),
                                            _u8(scale_b, "scale_b"),

@@ -36,7 +36,9 @@
 // one 3-D TMA box per operand (128 bytes x 128 rows x 2 blocks); the A and B
 // boxes are issued by two different warps.  One thread issues at most a few
 // million boxes a second whatever their size, so large boxes from two issuers
-// keep the issue rate well below that while 64 KB per stage is in flight.
+// keep the issue rate well below that while 64 KB per stage is in flight.  In
+// a masked unit whose second 128 rows all lie past masked_m[g], the peer CTA
+// fetches no A at all (those rows of the product are never stored).
 //
 // Warp roles per CTA (both CTAs run all roles except the MMA issue):
 //   warp 0  A producer: TMA of its 128 rows of A (completion counted on the

@@ -233,14 +233,21 @@ def run_once(fb, p, a, sa, b, sb, rowinfo, d, stream=None):
         fb.gemm_grouped_masked(a, sa, b, sb, d, rowinfo, stream=stream)
 
 
-def alloc_out(p, dev, pinned=False):
+def alloc_out(p, dev, pinned=False, d_offset_bytes=0):
     """The step's output: D (bf16/f16), or for the fused epilogue the E4M3 codes and
     their fp32 scales in the activation-scale layout of the workload.  Returns the
     argument run_once takes and the list of underlying tensors (on the device, or
-    in pinned host memory)."""
+    in pinned host memory).  d_offset_bytes > 0 places D that many bytes into a
+    larger buffer (a slice, as a caller's view of a bigger tensor would be)."""
     lead = (p.rows,) if p.variant == "contiguous" else (p.G, p.M_max)
     kw = {"pin_memory": True} if pinned else {"device": dev}
     if p.epilogue != "silu_mul_quant":
+        if d_offset_bytes:
+            numel = math.prod(lead) * p.N
+            off = d_offset_bytes // 2
+            buf = torch.empty(numel + off, dtype=out_dtype_of(p), **kw)
+            d = buf[off:].view(lead + (p.N,))
+            return d, [d]
         d = torch.empty(lead + (p.N,), dtype=out_dtype_of(p), **kw)
         return d, [d]
     q = torch.empty(lead + (p.N // 2,), dtype=torch.uint8, **kw)
@@ -306,7 +313,7 @@ def bench_ours(args):
                       else sa_store[:, :, : p.M_max].transpose(1, 2))
             else:
                 sa = sa_store
-        d, _ = alloc_out(p, dev)
+        d, _ = alloc_out(p, dev, d_offset_bytes=args.d_offset_bytes)
         bufs.append((a, sa, b, sb, ri, d))
     l2_note = (f"rotating {sets} input sets of {in_bytes / 1e6:.1f} MB "
                f"({sets * in_bytes / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)")
@@ -411,7 +418,9 @@ def bench_ours(args):
             "data": ("synthetic (seeded N(0,1), MXFP4-quantised)" if p.is_mx else
                      "synthetic (seeded N(0,1), fp32 block scales)" if p.scale_kind == "fp32" else
                      "synthetic (seeded N(0,1), UE8M0 ceil-quantised)"),
-            "config": describe(p, l2_note), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "config": dict(describe(p, l2_note),
+                           **({"d_offset_bytes": args.d_offset_bytes} if args.d_offset_bytes else {})),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "e2e_resident_weights": e2e_resident,
             "gpu_launches": args.steps, "clocks": clk,
             "roofline_time_ms": {"tensor_at_peak": tensor_time * 1e3, "hbm_at_peak": hbm_time * 1e3}}
@@ -600,6 +609,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--d-offset-bytes", type=int, default=0, choices=[0, 16],
+                    help="place D 16 bytes into a larger buffer (16- but not 32-byte aligned)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)

@@ -17,8 +17,10 @@ software instead of by the tensor core); the ``*_mxfp4`` entry points take both
 operands in MXFP4 (E2M1 with E8M0 scales per 32 elements).
 """
 from ._binding import (  # noqa: F401
+    DEBUG_SINGLE_CTA,
     DEBUG_STALL_MMA,
     DEVERR_BAD_GROUP,
+    DEVERR_BAD_SCALE,
     DEVERR_MASKED_M,
     DEVERR_MIXED_TILE,
     DEVERR_TIMEOUT,

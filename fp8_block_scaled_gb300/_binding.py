@@ -26,6 +26,7 @@ DEVERR_TIMEOUT = 0x1
 DEVERR_MASKED_M = 0x2
 DEVERR_MIXED_TILE = 0x4
 DEVERR_BAD_GROUP = 0x8
+DEVERR_BAD_SCALE = 0x10
 
 # every symbol include/fp8bs.h declares
 EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "gemm_grouped_contiguous_noalloc",
@@ -473,11 +474,13 @@ def device_error(device: int = None) -> int:
 
 
 DEBUG_STALL_MMA = 0x1
+DEBUG_SINGLE_CTA = 0x2
 
 
 def set_debug_flags(flags: int) -> None:
     """Test hook (include/fp8bs.h): DEBUG_STALL_MMA makes later pair-kernel launches
-    time out and abort on purpose; 0 turns it off."""
+    time out and abort on purpose; DEBUG_SINGLE_CTA routes the plain entry points to
+    the single-CTA kernel; 0 turns both off."""
     _check(load().fp8bs_set_debug_flags(int(flags)), "fp8bs_set_debug_flags")
 
 

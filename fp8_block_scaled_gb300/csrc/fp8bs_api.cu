@@ -250,6 +250,9 @@ int get_map3(int dev, const void* ptr, uint64_t inner, uint64_t outer, uint32_t 
 // grid has already freed); after a grid that never signals, or after a
 // non-kernel stream operation, the launch is ordered as usual.
 std::atomic<uint32_t> g_debug_flags{0};  // fp8bs_set_debug_flags (tests only)
+// FP8BS_DEBUG_SINGLE_CTA: host-side routing of the plain entry points to the
+// single-CTA kernel, so that tests can compare both kernels on one problem
+constexpr uint32_t kDebugSingleCta = 0x2u;
 
 inline void set_pdl(cudaLaunchAttribute& a) {
     a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -511,11 +514,14 @@ int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUte
         nd.max_clusters[slot] = clusters;
         nd.attr_set[slot] = true;
     }
-    const int64_t pairs = units_bound < nd.max_clusters[slot] ? units_bound : nd.max_clusters[slot];
+    // at most the pairs the array has stream-K slots for (2 each); a persistent grid of
+    // fewer pairs is as correct, only less parallel
+    int64_t pairs = units_bound < nd.max_clusters[slot] ? units_bound : nd.max_clusters[slot];
+    if (pairs > kNoAllocSlots / 2) pairs = kNoAllocSlots / 2;
     if (pairs <= 0) return FP8BS_OK;
-    if (2 * pairs > kNoAllocSlots) return FP8BS_ERR_INVALID_ARG;  // more pairs than the array holds
     // the slot counters must start at zero; a launch that gave up could have left
-    // them set, so clear them on the stream before every launch
+    // them set, so clear them on the stream before every launch (a non-kernel stream
+    // operation: the launch then cannot overlap the tail of the preceding kernel)
     uint32_t* flags = reinterpret_cast<uint32_t*>(nd.scratch + kNoAllocPartialBytes);
     if (cudaMemsetAsync(flags, 0, kNoAllocFlagBytes, stream) != cudaSuccess) {
         cudaGetLastError();
@@ -541,7 +547,7 @@ extern "C" {
 int fp8bs_abi_version(void) { return 1; }
 
 int fp8bs_set_debug_flags(uint32_t flags) {
-    if (flags & ~fp8bs::kDebugStallMma) return FP8BS_ERR_INVALID_ARG;
+    if (flags & ~(fp8bs::kDebugStallMma | kDebugSingleCta)) return FP8BS_ERR_INVALID_ARG;
     g_debug_flags.store(flags, std::memory_order_relaxed);
     return FP8BS_OK;
 }
@@ -588,8 +594,9 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     int dev = 0;
     cudaGetDevice(&dev);
     const int64_t m_tiles = (m_sum + 127) / 128;
-    bool pair = n % 256 == 0 && aligned(d, 32) && m_tiles <= fp8bs::kPairMaxTilesWs &&
-                num_groups < fp8bs::kPairMaxGroups;
+    bool pair = n % 256 == 0 && m_tiles <= fp8bs::kPairMaxTilesWs &&
+                num_groups < fp8bs::kPairMaxGroups &&
+                !(g_debug_flags.load(std::memory_order_relaxed) & kDebugSingleCta);
     // a pair list longer than shared memory holds goes to a device workspace; without
     // one (a first such call while capturing a graph) the single-CTA kernel runs
     PairList plist;
@@ -627,6 +634,7 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     p.raster_band = 8;
     p.list_ws = plist.buf;
     p.list_ws_stride = plist.stride;
+    p.d_align16 = aligned(d, 32) ? 0 : 1;
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
     if (pair)
         return dispatch_pair<false>(*st, out_dtype, *ta, *tb, p, tiles,
@@ -661,7 +669,8 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     if (rc != FP8BS_OK) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    const bool pair = n % 256 == 0 && aligned(d, 32);
+    const bool pair =
+        n % 256 == 0 && !(g_debug_flags.load(std::memory_order_relaxed) & kDebugSingleCta);
     const int bn = pair ? 256 : pick_bn(n);
     const CUtensorMap *ta = nullptr, *tb = nullptr;
     constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
@@ -692,6 +701,7 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     p.num_m_tiles = static_cast<int>((m_max + 127) / 128);
     p.num_n_tiles = static_cast<int>(n / bn);
     p.raster_band = 1;
+    p.d_align16 = aligned(d, 32) ? 0 : 1;
     if (pair) {
         const int64_t units = num_groups * ((m_max + 255) / 256) * p.num_n_tiles;
         return dispatch_pair<true>(*st, out_dtype, *ta, *tb, p, units,
@@ -1105,8 +1115,7 @@ int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_
     if (!grouped_layout || !aligned(grouped_layout, 4)) return FP8BS_ERR_INVALID_ARG;
     // only shapes the CTA-pair kernel takes
     const int64_t m_tiles = (m_sum + 127) / 128;
-    if (n % 256 != 0 || !aligned(d, 32) || m_tiles > fp8bs::kPairMaxTiles ||
-        num_groups >= fp8bs::kPairMaxGroups)
+    if (n % 256 != 0 || m_tiles > fp8bs::kPairMaxTiles || num_groups >= fp8bs::kPairMaxGroups)
         return FP8BS_ERR_INVALID_ARG;
 
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -1148,6 +1157,7 @@ int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_
     p.num_m_tiles = static_cast<int>(m_tiles);
     p.num_n_tiles = static_cast<int>(n / 256);
     p.raster_band = 8;
+    p.d_align16 = aligned(d, 32) ? 0 : 1;
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return out_dtype == FP8BS_OUT_BF16

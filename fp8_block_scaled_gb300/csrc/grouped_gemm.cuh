@@ -47,6 +47,7 @@ constexpr uint32_t kErrTimeout = 0x1u;
 constexpr uint32_t kErrMaskedM = 0x2u;
 constexpr uint32_t kErrMixedTile = 0x4u;
 constexpr uint32_t kErrBadGroup = 0x8u;
+constexpr uint32_t kErrBadScale = 0x10u;
 // GemmParams::debug_flags (test hook, 0 in normal use): the CTA-pair kernel's
 // MMA thread first waits on a barrier nothing arrives on, so its bounded wait
 // runs out and the launch takes the abort path.
@@ -80,6 +81,7 @@ struct GemmParams {
     int* list_ws;                // pair kernels: device pair list (list_ws_stride ints per
                                  // CTA) when it outgrows shared memory, else null
     int list_ws_stride;
+    int d_align16;               // pair kernel: d is 16- but not 32-byte aligned (16-byte stores)
 };
 
 template <int BN>
@@ -205,6 +207,18 @@ template <>
 __device__ __forceinline__ uint32_t pack2<__half>(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Whether an fp32 scale is a UE8M0 value: a positive power of two whose
+// exponent field the scale converters can take as the scale byte -- a normal
+// power of two (mantissa zero, exponent field 1..254, i.e. 2^-126..2^127) or
+// 2^-127, whose fp32 form is the subnormal 0x00400000 and whose exponent field
+// is 0, the UE8M0 code of 2^-127.  Anything else (another value, zero, a
+// negative or subnormal number, inf, NaN) would be truncated to a different
+// scale, so a stored row that reads one raises kErrBadScale.
+__device__ __forceinline__ bool ue8m0_scale_ok(uint32_t fbits) {
+    return ((fbits & 0x807FFFFFu) == 0u && fbits - 0x00800000u < 0x7F000000u) ||
+           fbits == 0x00400000u;
 }
 
 // fp32 power-of-two scale -> its exponent byte (the UE8M0 code), repeated in
@@ -443,12 +457,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
         // raw fp32 scales (row order) -> UE8M0 words in tcgen05.cp order:
         // word (lane*4 + c) holds row 32*c + lane; weight scales replicated
         // over their 128 columns.
+        // The scales of every row whose result is stored, and the tile's weight
+        // scales, are checked to be UE8M0 values (ue8m0_scale_ok); rows that are
+        // not computed may hold anything.
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
+        bool bad = false;
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
             const Tile tile = get_tile(t, false);
             if (tile.g < 0) continue;
+            uint32_t live = 0;  // bit q: row 32 q + lane of the tile is stored
+            int mm = 0;
+            if constexpr (kMasked) {
+                mm = __ldg(p.row_info + tile.g);
+                mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t m = static_cast<int64_t>(tile.m_tile) * kBM + q * 32 + lane;
+                bool stored;
+                if constexpr (kMasked) stored = m < mm;
+                else stored = m < p.rows && __ldg(p.row_info + m) == tile.g;
+                live |= stored ? 1u << q : 0u;
+            }
             for (int kb = 0; kb < KB; ++kb) {
                 if (!warp_wait_phase(bar_sf_raw(s), ph, abort_flag, p.err)) { ok = false; break; }
                 const uint32_t* raw = reinterpret_cast<const uint32_t*>(
@@ -459,6 +491,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 w.z = ue8m0_x4(raw[64 + lane]);
                 w.w = ue8m0_x4(raw[96 + lane]);
                 *reinterpret_cast<uint4*>(smem + L::kOffSfa + s * L::kSfaBytes + 16 * lane) = w;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    bad |= ((live >> q) & 1u) != 0u && !ue8m0_scale_ok(raw[32 * q + lane]);
                 const uint32_t* sbraw = reinterpret_cast<const uint32_t*>(
                     smem + L::kOffSbRaw + s * L::kSbRawBytes);
 #pragma unroll
@@ -467,12 +502,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     *reinterpret_cast<uint4*>(smem + L::kOffSfb + s * L::kSfbBytes + 512 * j +
                                               16 * lane) = make_uint4(v, v, v, v);
                 }
+                bad |= lane < BN / 128 && !ue8m0_scale_ok(sbraw[lane < BN / 128 ? lane : 0]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_sf_ready(s));
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
         }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(p.err, kErrBadScale);
     } else if (warp >= 4) {
         // ============================================================ epilogue
         const int q = warp & 3;                 // TMEM lane quadrant of this warp

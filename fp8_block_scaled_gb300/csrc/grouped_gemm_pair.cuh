@@ -938,17 +938,51 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (!aborted && prev_s >= 0) signal(prev_s, prev_ph);
     } else if (warp == 3) {
         // ============================================================ scale converter
+        // The activation scales of every row this CTA stores, and the unit's weight
+        // scales, are checked to be UE8M0 values (ue8m0_scale_ok): the conversion
+        // keeps only the exponent field.  Rows that are not computed may hold anything.
         int s = 0;
         uint32_t ph = 0;
+        bool bad = false;
         for (int pi = 0; !aborted; ++pi) {
             const PairPiece pc = get_piece(pi);
             if (pc.u < 0) break;
+            const PairUnit w = get_unit(pc.u);
+            uint32_t live = 0;  // bit q: row 32 q + lane of this CTA's half is stored
+            if (w.store) {
+                int mm = 0;
+                if constexpr (kMasked) {
+                    mm = __ldg(p.row_info + w.g);
+                    mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int64_t m = static_cast<int64_t>(w.m_base) + q * 32 + lane;
+                    bool stored;
+                    if constexpr (kMasked) stored = m < mm;
+                    else stored = m < p.rows && __ldg(p.row_info + m) == w.g;
+                    live |= stored ? 1u << q : 0u;
+                }
+            }
             for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
                 if (!pair_warp_wait(bar_sf_raw(s), ph, abort_flag, peer_abort, p.err)) {
                     aborted = true;
                     break;
                 }
                 if constexpr (!kMx) {
+#pragma unroll
+                    for (int j = 0; j < L::kKbPerStage; ++j) {
+                        if (ks * L::kKbPerStage + j < KB) {  // zero-filled past K
+                            const uint32_t* ra = reinterpret_cast<const uint32_t*>(
+                                smem + L::kOffSaRaw + (s * L::kKbPerStage + j) * L::kSaRawBytes);
+                            const uint32_t* rb = reinterpret_cast<const uint32_t*>(
+                                smem + L::kOffSbRaw + (s * L::kKbPerStage + j) * L::kSbRawBytes);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                bad |= ((live >> q) & 1u) != 0u && !ue8m0_scale_ok(ra[32 * q + lane]);
+                            bad |= lane < 2 && !ue8m0_scale_ok(rb[lane & 1]);
+                        }
+                    }
                     // One scale word per row (SFA) or column chunk (SFB) and stage: byte j
                     // is the UE8M0 scale of the stage's K block j, and the MMAs of K block j
                     // select byte j through the instruction's scale ids, so a stage needs
@@ -983,6 +1017,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
         }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(p.err, kErrBadScale);
     } else if (warp >= 4) {
         // ============================================================ epilogue
         const int q = warp & 3;
@@ -1060,15 +1095,16 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
                 if (valid) {
+                    const bool split = p.d_align16 != 0;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            st_global_v8(dst + 128 * c + 32 * i, packed[c][8 * i],
-                                         packed[c][8 * i + 1], packed[c][8 * i + 2],
-                                         packed[c][8 * i + 3], packed[c][8 * i + 4],
-                                         packed[c][8 * i + 5], packed[c][8 * i + 6],
-                                         packed[c][8 * i + 7]);
+                            st_global_32B(dst + 128 * c + 32 * i, split, packed[c][8 * i],
+                                          packed[c][8 * i + 1], packed[c][8 * i + 2],
+                                          packed[c][8 * i + 3], packed[c][8 * i + 4],
+                                          packed[c][8 * i + 5], packed[c][8 * i + 6],
+                                          packed[c][8 * i + 7]);
                         }
                     }
                 }
@@ -1181,9 +1217,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     if (valid) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            st_global_v8(dst + 128 * c + 32 * i, pk[8 * i], pk[8 * i + 1],
-                                         pk[8 * i + 2], pk[8 * i + 3], pk[8 * i + 4], pk[8 * i + 5],
-                                         pk[8 * i + 6], pk[8 * i + 7]);
+                            st_global_32B(dst + 128 * c + 32 * i, p.d_align16 != 0, pk[8 * i],
+                                          pk[8 * i + 1], pk[8 * i + 2], pk[8 * i + 3], pk[8 * i + 4],
+                                          pk[8 * i + 5], pk[8 * i + 6], pk[8 * i + 7]);
                         }
                     }
                 }

@@ -424,6 +424,26 @@ __device__ __forceinline__ void st_global_v8(void* ptr, uint32_t a0, uint32_t a1
                  : "memory");
 }
 
+__device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3)
+                 : "memory");
+}
+
+// 32 bytes of output: one 32-byte store, or two 16-byte stores when the
+// destination is only 16-byte aligned (split is uniform across the launch).
+__device__ __forceinline__ void st_global_32B(void* ptr, bool split, uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t a4, uint32_t a5,
+                                              uint32_t a6, uint32_t a7) {
+    if (split) {
+        st_global_v4(ptr, a0, a1, a2, a3);
+        st_global_v4(static_cast<uint8_t*>(ptr) + 16, a4, a5, a6, a7);
+    } else {
+        st_global_v8(ptr, a0, a1, a2, a3, a4, a5, a6, a7);
+    }
+}
+
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart (SBO),

@@ -16,8 +16,13 @@
  * Scales are fp32 values that must be powers of two in [2^-127, 2^127]
  * (UE8M0: the page's section "DeepGEMM conformance details" rounds them with
  * ceil_to_ue8m0 and has the matrix instruction apply them).  The kernels use
- * the fp32 exponent field as the UE8M0 scale byte; a scale that is not a
- * power of two is truncated to the power of two below it.
+ * the fp32 exponent field as the UE8M0 scale byte.  A call whose stored rows
+ * read any other scale value (not a power of two, zero, negative, inf or NaN)
+ * is invalid: the kernels check every scale that enters a stored row and set
+ * FP8BS_DEVERR_BAD_SCALE, and the rows that read such a scale hold
+ * undefined values.  Scales of rows that are not computed are not read for
+ * any result and are not checked.  For classic fp32 scales (amax / 448) use
+ * the *_fp32_scales entry points.
  *
  * Conventions shared by every entry point:
  *  - All tensor pointers are DEVICE pointers owned by the caller, row-major and
@@ -55,8 +60,9 @@
  *    are not written: D keeps its prior contents there.
  *  - Return value: FP8BS_OK, or an error code; nothing is enqueued on error.
  *    Device-side problems (masked_m out of range, a 128-row tile holding two
- *    experts, a pipeline wait that exceeded its time limit) are recorded in a
- *    per-device error word read by fp8bs_device_error().
+ *    experts, a scale that is not a UE8M0 value, a pipeline wait that exceeded
+ *    its time limit) are recorded in a per-device error word read by
+ *    fp8bs_device_error().
  */
 #ifndef FP8BS_H
 #define FP8BS_H
@@ -89,6 +95,9 @@ enum fp8bs_sa_layout {
 #define FP8BS_DEVERR_MASKED_M 0x2u      /* masked_m[g] < 0 or > M_max (clamped) */
 #define FP8BS_DEVERR_MIXED_TILE 0x4u    /* a 128-row tile held rows of two experts */
 #define FP8BS_DEVERR_BAD_GROUP 0x8u     /* grouped_layout value >= num_groups or < -1 */
+#define FP8BS_DEVERR_BAD_SCALE 0x10u    /* an E4M3-path scale of a stored row (or of its
+                                           weight block) is not a power of two in
+                                           [2^-127, 2^127] */
 
 /*
  * Contiguous grouped GEMM (DeepGEMM's m_grouped_fp8_gemm_nt_contiguous
@@ -275,20 +284,21 @@ int gemm_grouped_masked_mxfp4(const void* a, const uint8_t* scale_a, const void*
  * cudaMalloc'd workspace:
  *  - size: 160 slots of 128 x 256 fp32 (2 per CTA pair, up to 80 pairs) plus
  *    1280 bytes of counters, about 20 MiB; every GPU that loads the library
- *    holds it until the process exits;
+ *    holds it until the process exits.  A device that fits more than 80 CTA
+ *    pairs runs this entry point on 80 of them (same results);
  *  - the first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
  *    before capturing the stream into a CUDA graph;
  *  - every call clears the slot counters (cudaMemsetAsync on `stream`) and
- *    then launches; calls share the array, so calls that overlap on the GPU
- *    (for instance on two streams at once) race and give wrong results;
+ *    then launches, so unlike the other entry points its kernel does not
+ *    start early on SMs freed by the preceding kernel on the stream; calls
+ *    share the array, so calls that overlap on the GPU (for instance on two
+ *    streams at once) race and give wrong results;
  *  - no cudaMalloc, cudaFree or other allocating routine is called, and the
  *    TMA tensor maps are encoded on the stack for every call.
  * Returns FP8BS_ERR_INVALID_ARG, in addition to the cases of
  * gemm_grouped_contiguous, for shapes the CTA-pair kernel does not take
- * (n % 256 != 0, d not 32-byte aligned, m_sum > 524288 rows, num_groups >= 2^15)
- * and when the device would run more than 80 CTA pairs (more scratch than the
- * array holds).
+ * (n % 256 != 0, m_sum > 524288 rows, num_groups >= 2^15).
  */
 int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_layout,
                                     int64_t ld_sa, const void* b, const float* scale_b,
@@ -317,6 +327,12 @@ int fp8bs_clear_cache(void);
  * free tensor memory and exit) and FP8BS_DEVERR_TIMEOUT is recorded.  D is
  * then undefined.  Returns FP8BS_ERR_INVALID_ARG for unknown bits. */
 #define FP8BS_DEBUG_STALL_MMA 0x1u
+/* FP8BS_DEBUG_SINGLE_CTA routes later gemm_grouped_contiguous and
+ * gemm_grouped_masked calls to the single-CTA kernel (128-row tiles), which
+ * otherwise runs only when n % 256 != 0 or the pair list cannot be had: a
+ * cross-check of the two kernels on the same problem.  Results are within
+ * the same tolerances; nothing else changes. */
+#define FP8BS_DEBUG_SINGLE_CTA 0x2u
 int fp8bs_set_debug_flags(uint32_t flags);
 
 /* Library ABI version (1). */

@@ -436,9 +436,12 @@ def make_config(name: str, device="cpu") -> Problem:
 def sample_rows(p: Problem, per_group: int = 32, seed: int = 0):
     """Seeded row sample for checking a large problem row by row.
 
-    Per group: the first and last valid rows and ``per_group`` uniform random
-    valid rows (valid_rows); plus, per group, its first padding / masked row
-    when it has one (untouched_rows, which must keep their prior contents).
+    valid_rows, per group: the first and last valid rows, ``per_group`` uniform
+    random valid rows, and one random valid row of every 128-row tile of the
+    group (the kernels' row tiles: a contiguous expert starts on a tile
+    boundary, a masked group's tiles start at its row 0), so that every tile
+    the kernel computes is compared.  untouched_rows: every row that must keep
+    its prior contents (padding rows, rows past masked_m, the ragged tail).
     Indices are flattened rows of A (contiguous: global row; masked: g*M_max+m).
     """
     rng = np.random.default_rng(10_007 + seed)
@@ -449,10 +452,12 @@ def sample_rows(p: Problem, per_group: int = 32, seed: int = 0):
         if m > 0:
             picks = {0, m - 1}
             picks.update(int(v) for v in rng.integers(0, m, size=min(per_group, m)))
+            for t0 in range(0, m, 128):
+                picks.add(t0 + int(rng.integers(0, min(128, m - t0))))
             valid.extend(base + v for v in sorted(picks))
-        if span > m:
-            untouched.append(base + m)
-            untouched.append(base + span - 1)
+        untouched.extend(range(base + m, base + span))
+    if p.variant == "contiguous":
+        untouched.extend(range(p.row_offsets[-1], p.rows))  # ragged tail after the last group
     return (np.array(sorted(set(valid)), dtype=np.int64),
             np.array(sorted(set(untouched)), dtype=np.int64))
 

@@ -12,6 +12,8 @@ with bf16/f16 output):
 """
 from __future__ import annotations
 
+import contextlib
+
 import numpy as np
 import torch
 
@@ -144,3 +146,15 @@ def all_rows(p):
     for r in range(p.rows):
         (valid if p.group_of_row(r)[0] >= 0 else untouched).append(r)
     return np.array(valid, np.int64), np.array(untouched, np.int64)
+
+
+@contextlib.contextmanager
+def single_cta_kernel(on=True):
+    """Route the plain entry points to the single-CTA kernel (test hook) inside the block."""
+    if on:
+        fb.set_debug_flags(fb.DEBUG_SINGLE_CTA)
+    try:
+        yield
+    finally:
+        if on:
+            fb.set_debug_flags(0)

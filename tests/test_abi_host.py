@@ -54,6 +54,13 @@ def test_host_only_entry_points(lib):
     fb.clear_cache()
 
 
+def test_debug_flags_take_the_declared_bits_only(lib):
+    for flags in (fb.DEBUG_STALL_MMA, fb.DEBUG_SINGLE_CTA, fb.DEBUG_STALL_MMA | fb.DEBUG_SINGLE_CTA, 0):
+        assert lib.fp8bs_set_debug_flags(flags) == OK
+    assert lib.fp8bs_set_debug_flags(0x4) == INVALID
+    assert lib.fp8bs_set_debug_flags(0) == OK
+
+
 P = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
 
 
@@ -154,7 +161,7 @@ def _noalloc(**kw):
 
 @pytest.mark.parametrize("bad", [
     dict(n=384),                 # the CTA-pair kernel needs N % 256 == 0
-    dict(d=P + 16),              # and a 32-byte aligned D
+    dict(d=P + 8),               # D 16-byte aligned like every entry point's
     dict(m_sum=524288 + 128),    # and at most 4096 row tiles (no workspace for a longer list)
     dict(g=1 << 15),             # and fewer than 2^15 groups (15-bit expert id of a list entry)
     dict(a=0), dict(k=100), dict(out=5),

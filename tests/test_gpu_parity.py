@@ -17,7 +17,7 @@ import oracle
 import synth
 from synth.inputs import OUT_BF16, OUT_F16, SA_KM, SA_MK
 
-from _parity import SENTINEL, all_rows, compare, run_gpu
+from _parity import SENTINEL, all_rows, compare, run_gpu, single_cta_kernel
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -152,20 +152,27 @@ def test_hand_cases_exact_bits(gg, case):
             assert (bits[int(r), lo:hi] == int(hexbits, 16)).all(), (r, hex(int(bits[int(r), lo])))
 
 
-@pytest.mark.parametrize("d_offset", [0, 8])
-def test_device_flags_mixed_and_bad_groups(gg, d_offset):
+# (D offset in elements, single-CTA kernel): a 32-byte aligned D on the CTA-pair
+# kernel, a 16-byte aligned D on the CTA-pair kernel (its 16-byte stores), and the
+# single-CTA kernel (test hook)
+KERNELS = [pytest.param(0, False, id="pair"), pytest.param(8, False, id="pair_d16"),
+           pytest.param(0, True, id="single_cta")]
+
+
+@pytest.mark.parametrize("d_offset,single", KERNELS)
+def test_device_flags_mixed_and_bad_groups(gg, d_offset, single):
     """The first row of a 128-row tile names its expert (the contiguous layout
     pads every expert to a multiple of 128 rows).  A row of another expert
     inside a tile, and a group id out of range, are reported in the device
-    error word and left unwritten.  d_offset=8 elements makes D only 16-byte
-    aligned, which selects the single-CTA kernel; 0 selects the CTA-pair kernel."""
+    error word and left unwritten, by both kernels and with either D alignment."""
     p = synth.make_problem("contiguous", 2, 256, 256, [128, 128], seed=91, device=DEV)
     lay = p.grouped_layout.clone()
     lay[5] = 1            # tile 0 (expert 0) now holds a row of expert 1
     lay[200] = 7          # out of range in tile 1 (expert 1)
     buf = torch.full((256 * 256 + 16,), SENTINEL, dtype=torch.int16, device=DEV)
     d = buf[d_offset:d_offset + 256 * 256].view(torch.bfloat16).view(256, 256)
-    fb.gemm_grouped_contiguous(p.a, p.sa, p.b, p.sb, d, lay)
+    with single_cta_kernel(single):
+        fb.gemm_grouped_contiguous(p.a, p.sa, p.b, p.sb, d, lay)
     torch.cuda.synchronize()
     flags = fb.device_error()
     assert flags & fb.DEVERR_MIXED_TILE and flags & fb.DEVERR_BAD_GROUP
@@ -176,26 +183,57 @@ def test_device_flags_mixed_and_bad_groups(gg, d_offset):
     assert fb.device_error() == 0  # cleared by the read
 
 
-def test_single_cta_and_pair_kernels_agree(gg):
-    """The same N%256==0 problem through both kernels (D 32-byte aligned selects
-    the CTA-pair kernel, 16-byte aligned the single-CTA kernel) against the oracle."""
-    p = synth.make_problem("contiguous", 3, 512, 768, [100, 300, 257], sa_layout=SA_KM, seed=93,
-                           device=DEV)
-    shape = (p.rows, p.N)
+@pytest.mark.parametrize("variant", ["contiguous", "masked"])
+def test_single_cta_and_pair_kernels_agree(gg, variant):
+    """The same N%256==0 problem through the CTA-pair kernel with a 32-byte and a
+    16-byte aligned D (one 32-byte store or two 16-byte stores per 16 columns) and
+    through the single-CTA kernel, each against the oracle; the two pair runs are
+    bit-identical and the words around D are never written."""
+    if variant == "contiguous":
+        p = synth.make_problem("contiguous", 3, 512, 768, [100, 300, 257], sa_layout=SA_KM,
+                               seed=93, device=DEV)
+        shape = (p.rows, p.N)
+    else:
+        p = synth.make_problem("masked", 3, 512, 768, [100, 300, 257], M_max=320, sa_layout=SA_KM,
+                               seed=94, device=DEV)
+        shape = (p.G, p.M_max, p.N)
     numel = p.rows * p.N
     outs = []
-    for off in (0, 8):
-        buf = torch.full((numel + 16,), SENTINEL, dtype=torch.int16, device=DEV)
+    for off, single in ((0, False), (8, False), (0, True)):
+        buf = torch.full((numel + 32,), SENTINEL, dtype=torch.int16, device=DEV)
         d = buf[off:off + numel].view(torch.bfloat16).view(*shape)
-        fb.gemm_grouped_contiguous(p.a, p.sa_mk_view(), p.b, p.sb, d, p.grouped_layout)
+        with single_cta_kernel(single):
+            if variant == "contiguous":
+                fb.gemm_grouped_contiguous(p.a, p.sa_mk_view(), p.b, p.sb, d, p.grouped_layout)
+            else:
+                fb.gemm_grouped_masked(p.a, p.sa_mk_view(), p.b, p.sb, d, p.masked_m)
         torch.cuda.synchronize()
         assert fb.device_error() == 0
-        outs.append(d.view(torch.int16).cpu().numpy().view(np.uint16).reshape(shape))
+        whole = buf.cpu().numpy().view(np.uint16)
+        assert (whole[:off] == SENTINEL).all() and (whole[off + numel:] == SENTINEL).all()
+        outs.append(whole[off:off + numel].reshape(-1, p.N))
     valid, untouched = all_rows(p)
     for bits in outs:
         compare(p, bits, valid, untouched, check_fp32=False)
-    same = (outs[0] == outs[1]).mean()
-    assert same > 0.99
+    assert np.array_equal(outs[0], outs[1])
+    assert (outs[0] == outs[2]).mean() > 0.99
+
+
+def test_misaligned_d_at_full_size(gg):
+    """The headline workload with D only 16-byte aligned (a slice of a larger
+    buffer): the CTA-pair kernel with 16-byte stores, bit-identical to the
+    32-byte aligned run, every 128-row tile sampled against the oracle."""
+    p = synth.make_config("c2_contig_g8_m1024_n2048_k7168", device=DEV)
+    ref = run_gpu(p)
+    numel = p.rows * p.N
+    buf = torch.full((numel + 16,), SENTINEL, dtype=torch.int16, device=DEV)
+    d = buf[8:8 + numel].view(torch.bfloat16).view(p.rows, p.N)
+    bits = run_gpu(p, d=d)
+    assert np.array_equal(bits, ref)
+    assert (buf[:8].cpu().numpy().view(np.uint16) == SENTINEL).all()
+    assert (buf[8 + numel:].cpu().numpy().view(np.uint16) == SENTINEL).all()
+    valid, untouched = synth.sample_rows(p, per_group=8, seed=3)
+    compare(p, bits, valid, untouched, check_fp32=False)
 
 
 def test_masked_m_out_of_range_is_clamped_and_flagged(gg):

@@ -116,3 +116,21 @@ def test_mxfp4_quantiser_invariants():
     assert np.all(np.abs(np.abs(deq) - np.abs(y)) <= np.maximum(best, np.abs(y) - 6.0) + 1e-12)
     assert np.all((deq == 0) | (np.sign(deq) == np.sign(y)))
     assert np.all(codes[3] == 0)
+
+
+def test_sample_rows_cover_every_tile_and_all_untouched_rows():
+    """Every 128-row tile that holds a valid row contributes a sampled row, and
+    every row that must not be written is listed."""
+    for p in (synth.make_problem("contiguous", 3, 128, 128, [300, 0, 129], seed=4, tail_rows=20),
+              synth.make_problem("masked", 3, 128, 128, [0, 257, 130], M_max=300, seed=5)):
+        v, u = synth.sample_rows(p, per_group=2)
+        vs = set(v.tolist())
+        for r in range(p.rows):
+            g, m = p.group_of_row(r)
+            if g < 0:
+                assert r in set(u.tolist())
+        for g, m in enumerate(p.group_sizes):
+            base = p.row_offsets[g] if p.variant == "contiguous" else g * p.M_max
+            for t0 in range(0, m, 128):
+                assert any(base + t0 <= r < base + min(m, t0 + 128) for r in vs), (g, t0)
+        assert len(u) == p.rows - p.valid_rows

@@ -2,7 +2,9 @@
 allocate device memory (it keeps its scratch in a static device array of the
 library).  Through the C ABI, two calls in a row must match the allocating
 entry point gemm_grouped_contiguous within the parity tolerances of the other
-GPU tests.  This file is collected last on purpose."""
+GPU tests, and each call's valid rows must also meet those tolerances against
+the CPU oracle directly (a fault that both entry points shared would otherwise
+go unseen).  This file is collected last on purpose."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +15,7 @@ import synth
 from fp8_block_scaled_gb300 import _binding
 from synth.inputs import OUT_F16, SA_KM, SA_MK
 
-from _parity import CALC_DIFF_ORACLE, REL_TOL, RMS_TOL, SENTINEL, all_rows
+from _parity import CALC_DIFF_ORACLE, REL_TOL, RMS_TOL, SENTINEL, all_rows, compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -56,3 +58,4 @@ def test_noalloc_matches_allocating_entry_point_twice(gg, spec):
         assert oracle.calc_diff(got, ref) <= CALC_DIFF_ORACLE
         assert (np.abs(got - ref) <= REL_TOL * np.abs(ref) + RMS_TOL * rms).all()
         assert (bits[untouched] == SENTINEL).all()
+        compare(p, bits, valid, untouched, check_fp32=False)  # against the oracle itself

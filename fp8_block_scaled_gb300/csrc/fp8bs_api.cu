@@ -594,7 +594,7 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     int dev = 0;
     cudaGetDevice(&dev);
     const int64_t m_tiles = (m_sum + 127) / 128;
-    bool pair = n % 256 == 0 && m_tiles <= fp8bs::kPairMaxTilesWs &&
+    bool pair = m_tiles <= fp8bs::kPairMaxTilesWs &&
                 num_groups < fp8bs::kPairMaxGroups &&
                 !(g_debug_flags.load(std::memory_order_relaxed) & kDebugSingleCta);
     // a pair list longer than shared memory holds goes to a device workspace; without
@@ -630,7 +630,9 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     p.kb_count = static_cast<int>(k / 128);
     p.nb_count = static_cast<int>(n / 128);
     p.num_m_tiles = static_cast<int>((m_sum + 127) / 128);
-    p.num_n_tiles = static_cast<int>(n / bn);
+    // the pair kernel runs n % 256 == 128 with a 128-column last tile
+    p.num_n_tiles = static_cast<int>(pair ? (n + 255) / 256 : n / bn);
+    p.n_half = pair && n % 256 != 0 ? 1 : 0;
     p.raster_band = 8;
     p.list_ws = plist.buf;
     p.list_ws_stride = plist.stride;
@@ -669,8 +671,7 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     if (rc != FP8BS_OK) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    const bool pair =
-        n % 256 == 0 && !(g_debug_flags.load(std::memory_order_relaxed) & kDebugSingleCta);
+    const bool pair = !(g_debug_flags.load(std::memory_order_relaxed) & kDebugSingleCta);
     const int bn = pair ? 256 : pick_bn(n);
     const CUtensorMap *ta = nullptr, *tb = nullptr;
     constexpr uint32_t kKbBox = fp8bs::PairLayout::kKbPerStage;
@@ -699,7 +700,8 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     p.kb_count = static_cast<int>(kb);
     p.nb_count = static_cast<int>(n / 128);
     p.num_m_tiles = static_cast<int>((m_max + 127) / 128);
-    p.num_n_tiles = static_cast<int>(n / bn);
+    p.num_n_tiles = static_cast<int>(pair ? (n + 255) / 256 : n / bn);
+    p.n_half = pair && n % 256 != 0 ? 1 : 0;
     p.raster_band = 1;
     p.d_align16 = aligned(d, 32) ? 0 : 1;
     if (pair) {
@@ -1115,7 +1117,7 @@ int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_
     if (!grouped_layout || !aligned(grouped_layout, 4)) return FP8BS_ERR_INVALID_ARG;
     // only shapes the CTA-pair kernel takes
     const int64_t m_tiles = (m_sum + 127) / 128;
-    if (n % 256 != 0 || m_tiles > fp8bs::kPairMaxTiles || num_groups >= fp8bs::kPairMaxGroups)
+    if (m_tiles > fp8bs::kPairMaxTiles || num_groups >= fp8bs::kPairMaxGroups)
         return FP8BS_ERR_INVALID_ARG;
 
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -1155,7 +1157,8 @@ int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_
     p.kb_count = static_cast<int>(k / 128);
     p.nb_count = static_cast<int>(n / 128);
     p.num_m_tiles = static_cast<int>(m_tiles);
-    p.num_n_tiles = static_cast<int>(n / 256);
+    p.num_n_tiles = static_cast<int>((n + 255) / 256);
+    p.n_half = n % 256 != 0 ? 1 : 0;
     p.raster_band = 8;
     p.d_align16 = aligned(d, 32) ? 0 : 1;
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;

@@ -82,6 +82,7 @@ struct GemmParams {
                                  // CTA) when it outgrows shared memory, else null
     int list_ws_stride;
     int d_align16;               // pair kernel: d is 16- but not 32-byte aligned (16-byte stores)
+    int n_half;                  // pair kernel: n % 256 == 128, the last column tile is 128 wide
 };
 
 template <int BN>

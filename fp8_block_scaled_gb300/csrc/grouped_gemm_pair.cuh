@@ -265,6 +265,7 @@ struct PairUnit {
     int n_tile;   // 256-column tile
     int m_base;   // first row of this CTA's half (contiguous: global row; masked: row in group)
     bool store;   // this CTA's half belongs to the unit
+    bool half_n;  // the last column tile of an n % 256 == 128 problem: 128 columns wide
 };
 
 // Work units of one launch, the same on every CTA: contiguous -- the pair list
@@ -400,6 +401,7 @@ __device__ __forceinline__ PairUnit unit_of(const GemmParams& p, const int* list
         w.m_base = (local - w.n_tile * mp) * 2 * kBM + static_cast<int>(rank) * kBM;
         w.store = true;
     }
+    w.half_n = p.n_half != 0 && w.n_tile == p.num_n_tiles - 1;
     return w;
 }
 
@@ -499,6 +501,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     auto get_unit = [&](int u) { return unit_of<kMasked>(p, list, total_units, u, rank); };
 
     constexpr uint32_t kIdesc = make_idesc_mxf8(2 * kBM, 256);
+    constexpr uint32_t kIdescN128 = make_idesc_mxf8(2 * kBM, 128);  // 128-column tiles
     constexpr uint32_t kIdescMx0 = make_idesc_mxf4(2 * kBM, 256, 0);
     constexpr uint32_t kIdescMx2 = make_idesc_mxf4(2 * kBM, 256, 2);
     const int KB = p.kb_count;
@@ -568,9 +571,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     auto unit_rows = [&](const PairUnit& w, int64_t* a_row0, int* b_row0) {
         *a_row0 = kMasked ? static_cast<int64_t>(w.g) * p.rows + w.m_base
                           : static_cast<int64_t>(w.m_base);
-        // fused gate/up: the leader holds gate rows, the peer the matching up rows
+        // fused gate/up: the leader holds gate rows, the peer the matching up rows; a
+        // 128-column tile (half_n) gives each CTA 64 rows of B (its box loads 128, of
+        // which the MMA reads the first 64)
         *b_row0 = kSwiglu ? w.g * p.n + static_cast<int>(rank) * (p.n >> 1) + w.n_tile * 128
-                          : w.g * p.n + w.n_tile * 256 + static_cast<int>(rank) * 128;
+                          : w.g * p.n + w.n_tile * 256 + static_cast<int>(rank) * (w.half_n ? 64 : 128);
     };
 
     if (warp == 0 || warp == 2) {
@@ -654,9 +659,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                             cp_async_4(sa_dst + 4u * r, in ? src : p.sa, in ? 4u : 0u);
                         }
                         if (lane < 2) {
-                            const bool in = kb < KB;
-                            // the two 128-column chunks of the unit's B tile
+                            // the two 128-column chunks of the unit's B tile (a 128-column
+                            // tile has only the first; the second is zero)
                             const int nb = kSwiglu ? lane * (p.n >> 8) + w.n_tile : nb0 + lane;
+                            const bool in = kb < KB && nb < p.nb_count;
                             const float* src =
                                 p.sb + (static_cast<int64_t>(w.g) * p.nb_count + nb) * KB + kb;
                             cp_async_4(sbase + L::kOffSbRaw + (s * L::kKbPerStage + j) * L::kSbRawBytes +
@@ -727,6 +733,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     break;
                 }
                 tc_fence_after();
+                const uint32_t idesc_unit = (!kMx && get_unit(pc.u).half_n) ? kIdescN128 : kIdesc;
                 for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
                     if (!pair_wait(bar_full(s), ph, abort_flag, peer_abort, p.err)) {
                         aborted = true;
@@ -780,7 +787,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 tmem_base + sf0 + 8,
                                 make_desc_sf(sbase + L::kOffSfb + slot0 * L::kSfbBytes + 512));
                         }
-                        const uint32_t idesc_j = idesc_scale_ids(kIdesc, static_cast<uint32_t>(j));
+                        const uint32_t idesc_j = idesc_scale_ids(idesc_unit, static_cast<uint32_t>(j));
                         const uint64_t adesc = make_desc_sw128(sbase + L::kOffA + s * L::kAStageBytes +
                                                                j * L::kTileBytes);
                         const uint64_t bdesc = make_desc_sw128(sbase + L::kOffB + s * L::kBStageBytes +
@@ -980,7 +987,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
                                 bad |= ((live >> q) & 1u) != 0u && !ue8m0_scale_ok(ra[32 * q + lane]);
-                            bad |= lane < 2 && !ue8m0_scale_ok(rb[lane & 1]);
+                            // (a 128-column tile has no second weight-scale chunk)
+                            bad |= lane < (w.half_n ? 1 : 2) && !ue8m0_scale_ok(rb[lane & 1]);
                         }
                     }
                     // One scale word per row (SFA) or column chunk (SFB) and stage: byte j
@@ -1096,8 +1104,10 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (lane == 0) mbar_arrive_relaxed_cluster(empty_leader);
                 if (valid) {
                     const bool split = p.d_align16 != 0;
+                    const int nch = w.half_n ? 2 : 4;  // 64-column chunks of the tile
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
+                        if (c >= nch) break;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             st_global_32B(dst + 128 * c + 32 * i, split, packed[c][8 * i],
@@ -1214,7 +1224,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         pk[2 * i + 1] = pack2<OutT>(__uint_as_float(v[4 * i + 2]) + f.z,
                                                     __uint_as_float(v[4 * i + 3]) + f.w);
                     }
-                    if (valid) {
+                    if (valid && (c < 2 || !w.half_n)) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             st_global_32B(dst + 128 * c + 32 * i, p.d_align16 != 0, pk[8 * i],

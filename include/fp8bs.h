@@ -56,6 +56,10 @@
  *    it cannot be had, gemm_grouped_contiguous runs the one-CTA kernel
  *    instead (same results) and the other contiguous entry points return
  *    FP8BS_ERR_CUDA.
+ *  - Kernels: gemm_grouped_contiguous and gemm_grouped_masked run a CTA-pair
+ *    kernel (256 x 256 output tiles on two SMs) for every n; when n % 256 == 128
+ *    the last column tile is 128 wide.  D may be 16-byte aligned (32-byte
+ *    stores when it is 32-byte aligned, 16-byte stores otherwise).
  *  - Rows that are not computed (grouped_layout == -1, or m >= masked_m[g])
  *    are not written: D keeps its prior contents there.
  *  - Return value: FP8BS_OK, or an error code; nothing is enqueued on error.
@@ -298,7 +302,7 @@ int gemm_grouped_masked_mxfp4(const void* a, const uint8_t* scale_a, const void*
  *    TMA tensor maps are encoded on the stack for every call.
  * Returns FP8BS_ERR_INVALID_ARG, in addition to the cases of
  * gemm_grouped_contiguous, for shapes the CTA-pair kernel does not take
- * (n % 256 != 0, m_sum > 524288 rows, num_groups >= 2^15).
+ * (m_sum > 524288 rows, num_groups >= 2^15).
  */
 int gemm_grouped_contiguous_noalloc(const void* a, const float* scale_a, int sa_layout,
                                     int64_t ld_sa, const void* b, const float* scale_b,
@@ -329,7 +333,7 @@ int fp8bs_clear_cache(void);
 #define FP8BS_DEBUG_STALL_MMA 0x1u
 /* FP8BS_DEBUG_SINGLE_CTA routes later gemm_grouped_contiguous and
  * gemm_grouped_masked calls to the single-CTA kernel (128-row tiles), which
- * otherwise runs only when n % 256 != 0 or the pair list cannot be had: a
+ * otherwise runs only when the contiguous pair list cannot be had: a
  * cross-check of the two kernels on the same problem.  Results are within
  * the same tolerances; nothing else changes. */
 #define FP8BS_DEBUG_SINGLE_CTA 0x2u

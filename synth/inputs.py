@@ -72,6 +72,10 @@ CONFIGS: Dict[str, dict] = {
     "c9_mxfp4_contig_g8_m1024_n2048_k7168": dict(
         variant="contiguous", G=8, N=2048, K=7168, out=OUT_BF16, sa_layout=SA_MK,
         sizes=("fixed", 1024), seed=9, scale_kind="mxfp4"),
+    # workload 2's shape with N not a multiple of 256 (7.5 column tiles of 256)
+    "c10_contig_g8_m1024_n1920_k7168": dict(
+        variant="contiguous", G=8, N=1920, K=7168, out=OUT_BF16, sa_layout=SA_KM,
+        sizes=("fixed", 1024), seed=10),
 }
 
 

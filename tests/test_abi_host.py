@@ -160,7 +160,7 @@ def _noalloc(**kw):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(n=384),                 # the CTA-pair kernel needs N % 256 == 0
+    dict(n=200),                 # N a multiple of 128
     dict(d=P + 8),               # D 16-byte aligned like every entry point's
     dict(m_sum=524288 + 128),    # and at most 4096 row tiles (no workspace for a longer list)
     dict(g=1 << 15),             # and fewer than 2^15 groups (15-bit expert id of a list entry)

@@ -41,9 +41,10 @@ def _contiguous(n, seed):
                               device=DEV)
 
 
-# N % 256 == 0 runs the CTA-pair kernel; N=384, or the test hook, the single-CTA kernel
-KERNELS = [pytest.param(512, False, id="pair"), pytest.param(384, False, id="single_n384"),
-           pytest.param(512, True, id="single_hook")]
+# the CTA-pair kernel (N=384: its last column tile is 128 wide) and, through the
+# test hook, the single-CTA kernel
+KERNELS = [pytest.param(512, False, id="pair"), pytest.param(384, False, id="pair_n384"),
+           pytest.param(512, True, id="single_cta"), pytest.param(384, True, id="single_cta_n384")]
 
 
 @pytest.mark.parametrize("n,single", KERNELS)

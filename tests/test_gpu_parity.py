@@ -37,7 +37,7 @@ def test_config1_all_rows(gg):
 @pytest.mark.parametrize("out", [OUT_BF16, OUT_F16])
 def test_contiguous_ragged_multi_tile(gg, sa_layout, out):
     """Several m/n tiles, an empty expert, an expert spanning 3 tiles, a ragged
-    M_sum tail of -1 rows, N=384 (the 128-column tile path)."""
+    M_sum tail of -1 rows, N=384 (a 128-column last tile on the CTA-pair kernel)."""
     p = synth.make_problem("contiguous", 3, 384, 512, [130, 0, 300], out_dtype=out,
                            sa_layout=sa_layout, seed=31 + out, tail_rows=37, device=DEV)
     bits = run_gpu(p)
@@ -183,18 +183,19 @@ def test_device_flags_mixed_and_bad_groups(gg, d_offset, single):
     assert fb.device_error() == 0  # cleared by the read
 
 
+@pytest.mark.parametrize("n", [512, 384])
 @pytest.mark.parametrize("variant", ["contiguous", "masked"])
-def test_single_cta_and_pair_kernels_agree(gg, variant):
+def test_single_cta_and_pair_kernels_agree(gg, variant, n):
     """The same N%256==0 problem through the CTA-pair kernel with a 32-byte and a
     16-byte aligned D (one 32-byte store or two 16-byte stores per 16 columns) and
     through the single-CTA kernel, each against the oracle; the two pair runs are
     bit-identical and the words around D are never written."""
     if variant == "contiguous":
-        p = synth.make_problem("contiguous", 3, 512, 768, [100, 300, 257], sa_layout=SA_KM,
+        p = synth.make_problem("contiguous", 3, n, 768, [100, 300, 257], sa_layout=SA_KM,
                                seed=93, device=DEV)
         shape = (p.rows, p.N)
     else:
-        p = synth.make_problem("masked", 3, 512, 768, [100, 300, 257], M_max=320, sa_layout=SA_KM,
+        p = synth.make_problem("masked", 3, n, 768, [100, 300, 257], M_max=320, sa_layout=SA_KM,
                                seed=94, device=DEV)
         shape = (p.G, p.M_max, p.N)
     numel = p.rows * p.N
@@ -260,6 +261,18 @@ def test_stream_k_contiguous_all_rows_and_repeat(gg):
     compare(p, bits1, valid, untouched, check_fp32=False)
     bits2 = run_gpu(p)  # slot counters were reset by the first launch
     assert np.array_equal(bits1, bits2)
+
+
+def test_half_column_tile_with_stream_k(gg):
+    """N = 2432 = 9.5 column tiles of 256: the last tile of every row pair is 128 wide
+    (MMA N = 128, each CTA multiplying 64 rows of B), 80 units on 76 CTA pairs, so the
+    stream-K split also cuts half-width units."""
+    p = synth.make_problem("contiguous", 2, 2432, 1024, [1024, 1000], sa_layout=SA_KM, seed=104,
+                           device=DEV)
+    bits = run_gpu(p)
+    valid, untouched = all_rows(p)
+    compare(p, bits, valid, untouched, check_fp32=False)
+    assert np.array_equal(bits, run_gpu(p))
 
 
 def test_masked_many_units_all_rows(gg):

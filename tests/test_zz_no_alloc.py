@@ -39,10 +39,12 @@ PROBLEMS = [
     dict(G=2, N=2560, K=1024, sizes=[1024, 1000], sa_layout=SA_KM, out=0, seed=201),
     # ragged experts, f16 output, row-major activation scales
     dict(G=3, N=512, K=768, sizes=[100, 300, 257], sa_layout=SA_MK, out=OUT_F16, seed=202),
+    # N % 256 == 128: a 128-column last tile
+    dict(G=2, N=384, K=512, sizes=[300, 129], sa_layout=SA_KM, out=0, seed=203),
 ]
 
 
-@pytest.mark.parametrize("spec", PROBLEMS, ids=["streamk_80_units", "ragged_f16"])
+@pytest.mark.parametrize("spec", PROBLEMS, ids=["streamk_80_units", "ragged_f16", "n384"])
 def test_noalloc_matches_allocating_entry_point_twice(gg, spec):
     p = synth.make_problem("contiguous", spec["G"], spec["N"], spec["K"], spec["sizes"],
                            out_dtype=spec["out"], sa_layout=spec["sa_layout"], seed=spec["seed"],

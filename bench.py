@@ -300,7 +300,7 @@ def bench_ours(args):
     rowinfo = p.grouped_layout if p.variant == "contiguous" else p.masked_m
     in_bytes = sum(t.numel() * t.element_size() for t in (p.a, p.sa, p.b, p.sb, rowinfo))
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    sets = max(2, math.ceil(3 * l2 / in_bytes))
+    sets = args.input_sets or max(2, math.ceil(3 * l2 / in_bytes))
     bufs = []
     for i in range(sets):
         if i == 0:
@@ -609,6 +609,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--input-sets", type=int, default=0,
+                    help="rotating input sets (default: enough to exceed 3x L2, at least 2)")
     ap.add_argument("--d-offset-bytes", type=int, default=0, choices=[0, 16],
                     help="place D 16 bytes into a larger buffer (16- but not 32-byte aligned)")
     ap.add_argument("--e2e-steps", type=int, default=20)

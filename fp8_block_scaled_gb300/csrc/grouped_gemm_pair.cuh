@@ -733,7 +733,8 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     break;
                 }
                 tc_fence_after();
-                const uint32_t idesc_unit = (!kMx && get_unit(pc.u).half_n) ? kIdescN128 : kIdesc;
+                const uint32_t idesc_unit =
+                    (!kMx && p.n_half && get_unit(pc.u).half_n) ? kIdescN128 : kIdesc;
                 for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
                     if (!pair_wait(bar_full(s), ph, abort_flag, peer_abort, p.err)) {
                         aborted = true;
@@ -955,66 +956,62 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const PairPiece pc = get_piece(pi);
             if (pc.u < 0) break;
             const PairUnit w = get_unit(pc.u);
-            uint32_t live = 0;  // bit q: row 32 q + lane of this CTA's half is stored
-            if (w.store) {
-                int mm = 0;
-                if constexpr (kMasked) {
-                    mm = __ldg(p.row_info + w.g);
-                    mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
-                }
+            // whether row 32 q + lane of this CTA's half is stored: the row map is loaded
+            // here and first read by the checks after the piece's first arrival
+            int rmap[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int64_t m = static_cast<int64_t>(w.m_base) + q * 32 + lane;
-                    bool stored;
-                    if constexpr (kMasked) stored = m < mm;
-                    else stored = m < p.rows && __ldg(p.row_info + m) == w.g;
-                    live |= stored ? 1u << q : 0u;
-                }
+            for (int q = 0; q < 4; ++q) {
+                const int64_t m = static_cast<int64_t>(w.m_base) + q * 32 + lane;
+                if constexpr (kMasked) rmap[q] = q == 0 ? __ldg(p.row_info + w.g) : 0;
+                else rmap[q] = w.store && m < p.rows ? __ldg(p.row_info + m) : -1;
             }
+            auto stored = [&](int q) {
+                const int64_t m = static_cast<int64_t>(w.m_base) + q * 32 + lane;
+                if constexpr (kMasked) return w.store && m < rmap[0] && m < p.rows;
+                else return rmap[q] == w.g;
+            };
             for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
                 if (!pair_warp_wait(bar_sf_raw(s), ph, abort_flag, peer_abort, p.err)) {
                     aborted = true;
                     break;
                 }
+                // raw scales of this lane's rows (32 q + lane) and of the two weight chunks
+                uint32_t ra[L::kKbPerStage][4], rb[L::kKbPerStage];
                 if constexpr (!kMx) {
+                    const int slot0 = s * L::kKbPerStage;
 #pragma unroll
                     for (int j = 0; j < L::kKbPerStage; ++j) {
-                        if (ks * L::kKbPerStage + j < KB) {  // zero-filled past K
-                            const uint32_t* ra = reinterpret_cast<const uint32_t*>(
-                                smem + L::kOffSaRaw + (s * L::kKbPerStage + j) * L::kSaRawBytes);
-                            const uint32_t* rb = reinterpret_cast<const uint32_t*>(
-                                smem + L::kOffSbRaw + (s * L::kKbPerStage + j) * L::kSbRawBytes);
+                        const uint32_t* a_raw = reinterpret_cast<const uint32_t*>(
+                            smem + L::kOffSaRaw + (slot0 + j) * L::kSaRawBytes);
+                        const uint32_t* b_raw = reinterpret_cast<const uint32_t*>(
+                            smem + L::kOffSbRaw + (slot0 + j) * L::kSbRawBytes);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                bad |= ((live >> q) & 1u) != 0u && !ue8m0_scale_ok(ra[32 * q + lane]);
-                            // (a 128-column tile has no second weight-scale chunk)
-                            bad |= lane < (w.half_n ? 1 : 2) && !ue8m0_scale_ok(rb[lane & 1]);
-                        }
+                        for (int q = 0; q < 4; ++q) ra[j][q] = a_raw[32 * q + lane];
+                        rb[j] = b_raw[lane & 1];
                     }
                     // One scale word per row (SFA) or column chunk (SFB) and stage: byte j
                     // is the UE8M0 scale of the stage's K block j, and the MMAs of K block j
                     // select byte j through the instruction's scale ids, so a stage needs
                     // one set of scale copies instead of one per K block.
-                    const int slot0 = s * L::kKbPerStage;
-                    auto word = [&](int off_raw, int raw_bytes, int i) {
+                    auto word = [&](const uint32_t (&v)[L::kKbPerStage][4], int q) {
                         uint32_t w = 0;
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t* raw = reinterpret_cast<const uint32_t*>(
-                                smem + off_raw + (slot0 + j % L::kKbPerStage) * raw_bytes);
-                            w |= ((raw[i] >> 23) & 0xFFu) << (8 * j);
-                        }
+                        for (int j = 0; j < 4; ++j)
+                            w |= ((v[j % L::kKbPerStage][q] >> 23) & 0xFFu) << (8 * j);
                         return w;
                     };
                     uint4 wv;
-                    wv.x = word(L::kOffSaRaw, L::kSaRawBytes, lane);
-                    wv.y = word(L::kOffSaRaw, L::kSaRawBytes, 32 + lane);
-                    wv.z = word(L::kOffSaRaw, L::kSaRawBytes, 64 + lane);
-                    wv.w = word(L::kOffSaRaw, L::kSaRawBytes, 96 + lane);
+                    wv.x = word(ra, 0);
+                    wv.y = word(ra, 1);
+                    wv.z = word(ra, 2);
+                    wv.w = word(ra, 3);
                     *reinterpret_cast<uint4*>(smem + L::kOffSfa + slot0 * L::kSfaBytes + 16 * lane) = wv;
+                    uint32_t wb = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) wb |= ((rb[j % L::kKbPerStage] >> 23) & 0xFFu) << (8 * j);
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        const uint32_t v = word(L::kOffSbRaw, L::kSbRawBytes, c);
+                        const uint32_t v = __shfl_sync(0xffffffffu, wb, c);
                         *reinterpret_cast<uint4*>(smem + L::kOffSfb + slot0 * L::kSfbBytes + 512 * c +
                                                   16 * lane) = make_uint4(v, v, v, v);
                     }
@@ -1022,6 +1019,19 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_remote(mapa_shared(bar_full(s), 0));
+                if constexpr (!kMx) {
+                    // the checks come after the arrival: they delay no stage
+#pragma unroll
+                    for (int j = 0; j < L::kKbPerStage; ++j) {
+                        if (ks * L::kKbPerStage + j < KB) {  // zero-filled past K
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                bad |= stored(q) && !ue8m0_scale_ok(ra[j][q]);
+                            // (a 128-column tile has no second weight-scale chunk)
+                            bad |= lane < (w.half_n ? 1 : 2) && !ue8m0_scale_ok(rb[j]);
+                        }
+                    }
+                }
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
         }

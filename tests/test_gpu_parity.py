@@ -263,11 +263,12 @@ def test_stream_k_contiguous_all_rows_and_repeat(gg):
     assert np.array_equal(bits1, bits2)
 
 
-def test_half_column_tile_with_stream_k(gg):
+@pytest.mark.parametrize("k", [1024, 1152])
+def test_half_column_tile_with_stream_k(gg, k):
     """N = 2432 = 9.5 column tiles of 256: the last tile of every row pair is 128 wide
     (MMA N = 128, each CTA multiplying 64 rows of B), 80 units on 76 CTA pairs, so the
-    stream-K split also cuts half-width units."""
-    p = synth.make_problem("contiguous", 2, 2432, 1024, [1024, 1000], sa_layout=SA_KM, seed=104,
+    stream-K split also cuts half-width units; K = 1152 adds an odd count of K blocks."""
+    p = synth.make_problem("contiguous", 2, 2432, k, [1024, 1000], sa_layout=SA_KM, seed=104,
                            device=DEV)
     bits = run_gpu(p)
     valid, untouched = all_rows(p)

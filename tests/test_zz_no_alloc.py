@@ -21,9 +21,10 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(raw_fn, p):
+def _run(raw_fn, p, d_offset=0):
     numel = p.rows * p.N
-    buf = torch.full((numel,), SENTINEL, dtype=torch.int16, device=DEV)
+    full = torch.full((numel + 16,), SENTINEL, dtype=torch.int16, device=DEV)
+    buf = full[d_offset:d_offset + numel]
     d = buf.view(torch.bfloat16 if p.out_dtype == 0 else torch.float16)
     layout, ld = _binding._sa_layout_2d(p.sa_mk_view(), p.rows, p.KB)
     st = raw_fn(p.a.data_ptr(), p.sa.data_ptr(), layout, ld, p.b.data_ptr(), p.sb.data_ptr(),
@@ -31,6 +32,8 @@ def _run(raw_fn, p):
     assert st == 0, fb.status_string(st)
     torch.cuda.synchronize()
     assert fb.device_error() == 0
+    around = torch.cat([full[:d_offset], full[d_offset + numel:]]).cpu().numpy().view(np.uint16)
+    assert (around == SENTINEL).all(), "a word outside D was written"
     return buf.cpu().numpy().view(np.uint16).reshape(p.rows, p.N)
 
 
@@ -41,20 +44,23 @@ PROBLEMS = [
     dict(G=3, N=512, K=768, sizes=[100, 300, 257], sa_layout=SA_MK, out=OUT_F16, seed=202),
     # N % 256 == 128: a 128-column last tile
     dict(G=2, N=384, K=512, sizes=[300, 129], sa_layout=SA_KM, out=0, seed=203),
+    # D only 16-byte aligned (8 elements into its buffer): 16-byte stores
+    dict(G=2, N=512, K=512, sizes=[256, 200], sa_layout=SA_KM, out=0, seed=204, d_offset=8),
 ]
 
 
-@pytest.mark.parametrize("spec", PROBLEMS, ids=["streamk_80_units", "ragged_f16", "n384"])
+@pytest.mark.parametrize("spec", PROBLEMS, ids=["streamk_80_units", "ragged_f16", "n384", "d16"])
 def test_noalloc_matches_allocating_entry_point_twice(gg, spec):
     p = synth.make_problem("contiguous", spec["G"], spec["N"], spec["K"], spec["sizes"],
                            out_dtype=spec["out"], sa_layout=spec["sa_layout"], seed=spec["seed"],
                            device=DEV)
-    ref_bits = _run(_binding.gemm_grouped_contiguous_raw, p)
+    off = spec.get("d_offset", 0)
+    ref_bits = _run(_binding.gemm_grouped_contiguous_raw, p, off)
     valid, untouched = all_rows(p)
     ref = oracle.bits_to_float(ref_bits[valid], p.out_dtype)
     rms = float(np.sqrt(np.mean(ref ** 2)))
     for _ in range(2):
-        bits = _run(_binding.gemm_grouped_contiguous_noalloc_raw, p)
+        bits = _run(_binding.gemm_grouped_contiguous_noalloc_raw, p, off)
         got = oracle.bits_to_float(bits[valid], p.out_dtype)
         assert np.isfinite(got).all()
         assert oracle.calc_diff(got, ref) <= CALC_DIFF_ORACLE

@@ -9,17 +9,20 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <vector>
 
 #include "fp8bs.h"
 #include "grouped_gemm.cuh"
 #include "grouped_gemm_pair.cuh"
 #include "grouped_gemm_promote.cuh"
+#include "scale_pack.cuh"
 
 // Per-device error word written by the kernels (FP8BS_DEVERR_* bits).
 __device__ uint32_t g_fp8bs_error_word;
@@ -99,6 +102,12 @@ SkWorkspace* sk_workspace(int dev, cudaStream_t stream, int slots) {
     return &(g_sk[key] = w);
 }
 
+// Buffers of the per-stream workspaces below that a larger call replaced.  They are
+// kept, not freed, until the process exits: a CUDA graph captured while one of them
+// was current still points at it.  Growth at least doubles a workspace, so the kept
+// buffers add up to less than the current one.
+std::vector<void*> g_retired;
+
 // Device pair list of a contiguous problem whose row tiles outnumber the kernel's
 // shared-memory list: one region of `stride` ints per CTA of a grid of at most `ctas`
 // CTAs, kept per (device, stream) and grown on demand -- not while the stream is
@@ -125,18 +134,19 @@ bool pair_list_workspace(int dev, cudaStream_t stream, int ctas, int64_t m_tiles
             cudaGetLastError();
             return false;
         }
-        if (it != g_list.end()) {
-            cudaStreamSynchronize(stream);
-            cudaFree(it->second.buf);
-            g_list.erase(it);
-        }
+        const int64_t size = it == g_list.end() ? ints : std::max(ints, 2 * it->second.ints);
         ListWorkspace w;
-        if (cudaMalloc(&w.buf, sizeof(int) * ints) != cudaSuccess) {
+        if (cudaMalloc(&w.buf, sizeof(int) * size) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
-        w.ints = ints;
-        it = g_list.emplace(key, w).first;
+        w.ints = size;
+        if (it != g_list.end()) {
+            g_retired.push_back(it->second.buf);
+            it->second = w;
+        } else {
+            it = g_list.emplace(key, w).first;
+        }
     }
     out->buf = it->second.buf;
     out->stride = static_cast<int>(stride);
@@ -144,6 +154,38 @@ bool pair_list_workspace(int dev, cudaStream_t stream, int ctas, int64_t m_tiles
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Scale images of the E4M3 CTA-pair kernel (scale_pack.cuh), one buffer per
+// (device, stream) like the stream-K scratch: launches on one stream run one after
+// another (the pre-pass of the next call waits for the GEMM before it), launches on
+// different streams may overlap and must not share it.  Grown on demand like the
+// pair list, not while the stream is capturing a graph (cudaMalloc is not
+// captured): then the GEMM converts the fp32 scales itself (same results).
+struct PackWorkspace {
+    uint32_t* buf = nullptr;
+    int64_t words = 0;
+};
+std::map<std::pair<int, void*>, PackWorkspace> g_pack;
+
+uint32_t* pack_workspace(int dev, cudaStream_t stream, int64_t words) {
+    auto key = std::make_pair(dev, static_cast<void*>(stream));
+    auto it = g_pack.find(key);
+    if (it != g_pack.end() && it->second.words >= words) return it->second.buf;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    const int64_t size = it == g_pack.end() ? words : std::max(words, 2 * it->second.words);
+    PackWorkspace w;
+    if (cudaMalloc(&w.buf, sizeof(uint32_t) * size) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    w.words = size;
+    if (it != g_pack.end()) g_retired.push_back(it->second.buf);
+    return (g_pack[key] = w).buf;
+}
 
 // Resolve the current device and its cached state (lock held by caller).
 int device_state(DeviceState** out) {
@@ -257,6 +299,60 @@ constexpr uint32_t kDebugSingleCta = 0x2u;
 inline void set_pdl(cudaLaunchAttribute& a) {
     a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     a.val.programmaticStreamSerializationAllowed = 1;
+}
+
+// Makes the scale images of an E4M3 pair-kernel call and points `p` at them; with
+// no workspace to be had, leaves `p` without them (the kernel converts the fp32
+// scales itself).  Only for row-major activation scales: there the kernel's own
+// fetch is a gather of 4-byte values a row stride apart (one memory request per
+// row and K block), which the images turn into three contiguous 512-byte copies a
+// step; a transposed layout already gives contiguous 512-byte rows, and the extra
+// launch (which must wait for the previous kernel) costs more than it saves.
+// p.sa/sb/row_info, strides, rows, kb_count, nb_count, num_groups and num_m_tiles
+// must be set.
+int prepare_scale_images(DeviceState& st, int dev, GemmParams& p, bool masked, cudaStream_t stream) {
+    if (p.sa_row_stride == 1) return FP8BS_OK;  // transposed, or one K block
+    const int steps = (p.kb_count + fp8bs::PairLayout::kKbPerStage - 1) / fp8bs::PairLayout::kKbPerStage;
+    const int64_t tiles = masked ? static_cast<int64_t>(p.num_groups) * p.num_m_tiles : p.num_m_tiles;
+    const int64_t a_words = tiles * steps * 128;
+    const int64_t b_words = static_cast<int64_t>(p.num_groups) * p.nb_count * steps * 128;
+    uint32_t* buf = pack_workspace(dev, stream, a_words + b_words);
+    if (buf == nullptr) return FP8BS_OK;
+    fp8bs::ScalePackParams q{};
+    q.sa = p.sa;
+    q.sb = p.sb;
+    q.row_info = p.row_info;
+    q.packed_a = buf;
+    q.packed_b = buf + a_words;
+    q.err = p.err;
+    q.rows = p.rows;
+    q.sa_g_stride = p.sa_g_stride;
+    q.sa_kb_stride = p.sa_kb_stride;
+    q.sa_row_stride = p.sa_row_stride;
+    q.a_words = a_words;
+    q.b_words = b_words;
+    q.kb_count = p.kb_count;
+    q.steps = steps;
+    q.tiles_per_group = p.num_m_tiles;
+    q.masked = masked ? 1 : 0;
+    const int64_t blocks = (a_words + b_words + 255) / 256;
+    const int64_t max_blocks = static_cast<int64_t>(st.sms) * 8;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    set_pdl(attr[0]);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks < max_blocks ? blocks : max_blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fp8bs::scale_pack_kernel, q) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    p.sf_a_packed = q.packed_a;
+    p.sf_b_packed = q.packed_b;
+    p.sf_steps = steps;
+    return FP8BS_OK;
 }
 
 template <int BN, typename OutT, bool kMasked>
@@ -638,9 +734,12 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
     p.list_ws_stride = plist.stride;
     p.d_align16 = aligned(d, 32) ? 0 : 1;
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
-    if (pair)
+    if (pair) {
+        if ((rc = prepare_scale_images(*st, dev, p, false, static_cast<cudaStream_t>(stream))) != FP8BS_OK)
+            return rc;
         return dispatch_pair<false>(*st, out_dtype, *ta, *tb, p, tiles,
                                     static_cast<cudaStream_t>(stream));
+    }
     return dispatch<false>(*st, bn, out_dtype, *ta, *tb, p, tiles,
                            static_cast<cudaStream_t>(stream));
 }
@@ -706,6 +805,8 @@ int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int6
     p.d_align16 = aligned(d, 32) ? 0 : 1;
     if (pair) {
         const int64_t units = num_groups * ((m_max + 255) / 256) * p.num_n_tiles;
+        if ((rc = prepare_scale_images(*st, dev, p, true, static_cast<cudaStream_t>(stream))) != FP8BS_OK)
+            return rc;
         return dispatch_pair<true>(*st, out_dtype, *ta, *tb, p, units,
                                    static_cast<cudaStream_t>(stream));
     }
@@ -787,6 +888,8 @@ int gemm_grouped_contiguous_silu_mul_quant(const void* a, const float* scale_a, 
     p.qs_col_stride = out_scale_layout == FP8BS_SA_KM ? ld_out_scale : 1;
     p.list_ws = plist.buf;
     p.list_ws_stride = plist.stride;
+    if ((rc = prepare_scale_images(*st, dev, p, false, static_cast<cudaStream_t>(stream))) != FP8BS_OK)
+        return rc;
     return launch_pair<__nv_bfloat16, false, true>(*st, 24, *ta, *tb, p,
                                                    m_tiles * p.num_n_tiles,
                                                    static_cast<cudaStream_t>(stream));
@@ -850,6 +953,8 @@ int gemm_grouped_masked_silu_mul_quant(const void* a, const float* scale_a, int 
     p.qs_row_stride = out_scale_layout == FP8BS_SA_KM ? 1 : blocks;
     p.qs_col_stride = out_scale_layout == FP8BS_SA_KM ? ld_out_scale : 1;
     const int64_t units = num_groups * ((m_max + 255) / 256) * blocks;
+    if ((rc = prepare_scale_images(*st, dev, p, true, static_cast<cudaStream_t>(stream))) != FP8BS_OK)
+        return rc;
     return launch_pair<__nv_bfloat16, true, true>(*st, 25, *ta, *tb, p, units,
                                                   static_cast<cudaStream_t>(stream));
 }

@@ -83,6 +83,11 @@ struct GemmParams {
     int list_ws_stride;
     int d_align16;               // pair kernel: d is 16- but not 32-byte aligned (16-byte stores)
     int n_half;                  // pair kernel: n % 256 == 128, the last column tile is 128 wide
+    // pair kernel, E4M3: the scale images of scale_pack_kernel (null: the kernel gathers
+    // and converts the fp32 scales itself), with sf_steps pipeline steps per unit
+    const uint32_t* sf_a_packed;
+    const uint32_t* sf_b_packed;
+    int sf_steps;
 };
 
 template <int BN>

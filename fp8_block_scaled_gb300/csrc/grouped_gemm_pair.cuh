@@ -466,7 +466,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // scale converters
             mbar_init(bar_full(s), 4);
             mbar_init(bar_empty(s), 1);      // leader's multicast commit
-            mbar_init(bar_sf_raw(s), 32);    // own producer lanes' cp.async arrivals
+            // own A producer: 32 lanes' cp.async arrivals, or lane 1's arrival and the
+            // bytes of its bulk copies of packed scale images
+            mbar_init(bar_sf_raw(s), (!kMx && p.sf_a_packed != nullptr) ? 1 : 32);
         }
         mbar_init(bar_tmem_full, 1);
         mbar_init(bar_tmem_empty, 8);        // 4 epilogue warps x 2 CTAs
@@ -642,7 +644,33 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     }
                     if (pf) tma_prefetch_3d(map, 0, prow, kp * L::kKbPerStage);
                 }
-                if (is_a && !kMx) {
+                if (is_a && !kMx && p.sf_a_packed != nullptr) {
+                    // the stage's scale images, made by the scale pre-pass: 512 bytes of
+                    // SFA for the CTA's 128 rows and 512 bytes for each of the unit's two
+                    // weight-scale chunks, copied as they are (lane 1; lane 0 issues the
+                    // operand box)
+                    if (lane == 1) {
+                        // a CTA half past the last tile (the idle half of an odd pair, or of a
+                        // masked pair past m_max) copies the last tile's image: its rows are
+                        // never stored
+                        const int tl = min(w.m_base / kBM, p.num_m_tiles - 1);
+                        const int64_t t = kMasked ? static_cast<int64_t>(w.g) * p.num_m_tiles + tl : tl;
+                        const int gnb = w.g * p.nb_count;
+                        const int c0 = kSwiglu ? w.n_tile : w.n_tile * 2;
+                        // a 128-column tile has no second chunk: its image stands in (unused)
+                        const int c1 = kSwiglu ? (p.n >> 8) + w.n_tile : min(w.n_tile * 2 + 1, p.nb_count - 1);
+                        const uint32_t rb = bar_sf_raw(s);
+                        mbar_arrive_expect_tx(rb, 3u * 512u);
+                        bulk_load(sbase + L::kOffSfa + s * L::kKbPerStage * L::kSfaBytes,
+                                  p.sf_a_packed + (t * p.sf_steps + ks) * 128, 512u, rb);
+                        bulk_load(sbase + L::kOffSfb + s * L::kKbPerStage * L::kSfbBytes,
+                                  p.sf_b_packed + (static_cast<int64_t>(gnb + c0) * p.sf_steps + ks) * 128,
+                                  512u, rb);
+                        bulk_load(sbase + L::kOffSfb + s * L::kKbPerStage * L::kSfbBytes + 512,
+                                  p.sf_b_packed + (static_cast<int64_t>(gnb + c1) * p.sf_steps + ks) * 128,
+                                  512u, rb);
+                    }
+                } else if (is_a && !kMx) {
                     // raw scales of the stage's K blocks (zero beyond K and past the rows)
 #pragma unroll
                     for (int j = 0; j < L::kKbPerStage; ++j) {
@@ -956,6 +984,35 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const PairPiece pc = get_piece(pi);
             if (pc.u < 0) break;
             const PairUnit w = get_unit(pc.u);
+            if (p.sf_a_packed != nullptr && !kMx) {
+                // packed scale images: relay the stage's arrival to the leader's full
+                // barrier.  The step's four weight scales (lanes 0-3: chunk lane / 2, K
+                // block lane % 2) are checked after the next arrival, one step after
+                // their load was issued, so that the check never holds up a relay.
+                auto load_sb = [&](int ks) {
+                    const int c = lane >> 1;
+                    const int kb = ks * L::kKbPerStage + (lane & 1);
+                    const int nb = kSwiglu ? c * (p.n >> 8) + w.n_tile : w.n_tile * 2 + c;
+                    const bool chk = lane < (w.half_n ? 2 : 4) && kb < KB;
+                    return chk ? __float_as_uint(
+                                     __ldg(p.sb + (static_cast<int64_t>(w.g) * p.nb_count + nb) * KB + kb))
+                               : 0x3F800000u;  // 1.0: nothing to check
+                };
+                uint32_t sbv = load_sb(pc.ks0);
+                for (int ks = pc.ks0; ks < pc.ks1; ++ks) {
+                    if (!pair_warp_wait(bar_sf_raw(s), ph, abort_flag, peer_abort, p.err)) {
+                        aborted = true;
+                        break;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_remote(mapa_shared(bar_full(s), 0));
+                    const uint32_t cur = sbv;
+                    if (ks + 1 < pc.ks1) sbv = load_sb(ks + 1);
+                    bad |= !ue8m0_scale_ok(cur);
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
+                continue;
+            }
             // whether row 32 q + lane of this CTA's half is stored: the row map is loaded
             // here and first read by the checks after the piece's first arrival
             int rmap[4];

@@ -56,6 +56,18 @@
  *    it cannot be had, gemm_grouped_contiguous runs the one-CTA kernel
  *    instead (same results) and the other contiguous entry points return
  *    FP8BS_ERR_CUDA.
+ *  - Scale images: with row-major activation scales (sa_layout FP8BS_SA_MK
+ *    and k > 128), gemm_grouped_contiguous, gemm_grouped_masked and the two
+ *    *_silu_mul_quant entry points launch a short kernel before the GEMM that
+ *    writes the call's scales as the UE8M0 bytes the tensor core reads, in a
+ *    third per-stream workspace of (128-row tiles + num_groups * n/128) *
+ *    ceil(k/256) * 512 bytes, allocated the same way.  When it cannot be had
+ *    the GEMM converts the fp32 scales itself (same results).
+ *  - A per-stream workspace that a larger call outgrows is replaced by one at
+ *    least twice its size; the old buffer is kept, not freed, until exit, so a
+ *    CUDA graph captured while it was current stays valid.  A graph keeps
+ *    using the workspaces of the stream it was captured on: do not replay it
+ *    on another stream while calls run on that one.
  *  - Kernels: gemm_grouped_contiguous and gemm_grouped_masked run a CTA-pair
  *    kernel (256 x 256 output tiles on two SMs) for every n; when n % 256 == 128
  *    the last column tile is 128 wide.  D may be 16-byte aligned (32-byte

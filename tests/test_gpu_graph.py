@@ -1,6 +1,9 @@
 """CUDA-graph capture of the C-ABI calls: a launch captured on a stream that
 has already run the op (so its stream-K workspace exists) replays to the same
-bits as the eager launch, and the masked variant replays correctly too."""
+bits as the eager launch, and the masked variant replays correctly too.  The
+per-stream workspaces (stream-K scratch, scale images of row-major activation
+scales) are not allocated during a capture, and one that a later, larger call
+on the stream grows keeps the buffer an earlier capture points at."""
 import numpy as np
 import pytest
 import torch
@@ -8,7 +11,7 @@ import torch
 import fp8_block_scaled_gb300 as fb
 import synth
 
-from _parity import all_rows, compare
+from _parity import SENTINEL, all_rows, compare
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -56,3 +59,51 @@ def test_masked_graph_replay(gg):
     assert fb.device_error() == 0
     valid, untouched = all_rows(p)
     compare(p, _bits(d), valid, untouched)
+
+
+def test_capture_on_a_fresh_stream_matches_eager(gg):
+    """Nothing allocated on the stream yet (the first stream of torch's
+    high-priority pool, which no other test uses): the captured call runs without
+    the stream-K split and without scale images.  The split changes the order of
+    the fp32 sums, so the replay is held to the oracle, not to the eager bits."""
+    p = synth.make_problem("contiguous", 2, 2560, 512, [1024, 1000], seed=703, device=DEV)
+    d_graph = torch.full((p.rows, p.N), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    s = torch.cuda.Stream(priority=-1)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fb.gemm_grouped_contiguous(p.a, p.sa_mk_view(), p.b, p.sb, d_graph, p.grouped_layout)
+    g.replay()
+    torch.cuda.synchronize()
+    assert fb.device_error() == 0
+    valid, untouched = all_rows(p)
+    compare(p, _bits(d_graph), valid, untouched)
+
+
+def test_graph_replays_after_the_workspace_grew(gg):
+    small = synth.make_problem("contiguous", 2, 512, 512, [200, 150], seed=704, device=DEV)
+    large = synth.make_problem("contiguous", 4, 1024, 2048, [1024, 900, 700, 1024], seed=705,
+                               device=DEV)
+    s = torch.cuda.Stream(priority=-1)  # a stream no earlier call made large workspaces for
+    d_small = torch.zeros((small.rows, small.N), dtype=torch.bfloat16, device=DEV)
+    d_graph = torch.zeros_like(d_small)
+    d_large = torch.zeros((large.rows, large.N), dtype=torch.bfloat16, device=DEV)
+    with torch.cuda.stream(s):
+        fb.gemm_grouped_contiguous(small.a, small.sa_mk_view(), small.b, small.sb, d_small,
+                                   small.grouped_layout)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fb.gemm_grouped_contiguous(small.a, small.sa_mk_view(), small.b, small.sb, d_graph,
+                                   small.grouped_layout)
+    with torch.cuda.stream(s):  # needs larger scale images: the workspace grows
+        fb.gemm_grouped_contiguous(large.a, large.sa_mk_view(), large.b, large.sb, d_large,
+                                   large.grouped_layout)
+    s.synchronize()
+    for _ in range(2):
+        d_graph.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(_bits(d_graph), _bits(d_small))
+    assert fb.device_error() == 0
+    valid, untouched = all_rows(large)
+    compare(large, _bits(d_large), valid, untouched)

@@ -66,11 +66,12 @@ def test_masked_ragged(gg, sa_layout, n):
     compare(p, bits, valid, untouched)
 
 
-def test_masked_m_at_half_tile_edges(gg):
+@pytest.mark.parametrize("sa_layout", [SA_MK, SA_KM])
+def test_masked_m_at_half_tile_edges(gg, sa_layout):
     """masked_m just below, at and above multiples of 128: the pairs whose second
     128 rows hold no computed row (masked_m % 256 in [1, 128]) load no A there."""
     sizes = [128, 129, 256, 257, 384, 385, 511, 512]
-    p = synth.make_problem("masked", len(sizes), 512, 512, sizes, M_max=512, sa_layout=SA_KM,
+    p = synth.make_problem("masked", len(sizes), 512, 512, sizes, M_max=512, sa_layout=sa_layout,
                            seed=57, device=DEV)
     bits = run_gpu(p)
     valid, untouched = all_rows(p)

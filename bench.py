@@ -329,32 +329,36 @@ def bench_ours(args):
         clocks = ClockSampler(local)
         clocks.start()
         time.sleep(0.3)
-        # A step is exactly one launch of the kernel, so the kernel's average launch
-        # duration is the timed region's event time over the step count.  Events
-        # recorded between the launches would stand between two kernels of the
-        # stream and keep the next grid from being scheduled while the previous one
-        # finishes (programmatic dependent launch), so there are none.
+        # A step is one call: one launch of the GEMM, preceded, for row-major
+        # activation scales, by the library's scale pre-pass.  The GEMM's average
+        # launch duration is taken as the timed region's event time over the step
+        # count, which includes the pre-pass where there is one.  Events recorded
+        # between the launches would stand between two kernels of the stream and
+        # keep the next grid from being scheduled while the previous one finishes
+        # (programmatic dependent launch), so there are none.
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize(dev)
+        n0 = fb.kernel_launches()
         t0.record(stream)
         for i in range(args.steps):
             run_once(fb, p, *bufs[i % sets])
         t1.record(stream)
+        launches = fb.kernel_launches() - n0
         torch.cuda.synchronize(dev)
         barrier(world)
         clk = clocks.stop()
         if fb.device_error(local):
             raise RuntimeError("device error word set during the timed region")
-        return t0.elapsed_time(t1), clk
+        return t0.elapsed_time(t1), clk, launches
 
-    elapsed_ms, clk = timed_region()
+    elapsed_ms, clk, launches = timed_region()
     # a run slowed by the hardware or a thermal limit, or with the SM clock stuck
     # well below its maximum for no reported reason (a clock lock left by someone
     # else), is not kept: it is measured once more (a power-cap slowdown is kept)
     if max_over_ranks(1.0 if clocks_suspect(clk) else 0.0, world, dev) > 0.0:
-        elapsed_ms, clk = timed_region()
+        elapsed_ms, clk, launches = timed_region()
         clk["remeasured"] = True
     ms_per_step = max_over_ranks(elapsed_ms / args.steps, world, dev)
     flops = p.flops()
@@ -363,7 +367,8 @@ def bench_ours(args):
 
     # roofline of the one kernel on the path
     peaks, peaks_kind = load_peaks()
-    mean_launch_ms = elapsed_ms / args.steps
+    mean_launch_ms = elapsed_ms / args.steps  # with the scale pre-pass, if the step has one
+    kernels_per_step = launches / args.steps
     achieved = flops / (mean_launch_ms * 1e-3) / 1e12
     # the contraction's own dtype: E4M3 (or E2M1 for the MXFP4 workloads)
     ratio, ratio_name = ((FP4_OVER_BF16, "fp4/bf16") if p.is_mx else (FP8_OVER_BF16, "fp8/bf16"))
@@ -384,14 +389,14 @@ def bench_ours(args):
                 "peak_source": f"{peaks_kind} bf16 burst {peaks['bf16_tflops']} TFLOP/s x "
                                f"{ratio:g} (nominal {ratio_name} ratio)",
                 "algorithmic": {"flops_per_launch": flops, "bytes_per_launch": alg_bytes},
-                "mean_launch_ms": round(mean_launch_ms, 5)}
+                "mean_launch_ms": round(mean_launch_ms, 5), "kernels_per_step": kernels_per_step}
     else:
         gbs = alg_bytes / (mean_launch_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "peak_source": f"{peaks_kind} HBM copy",
                 "algorithmic": {"flops_per_launch": flops, "bytes_per_launch": alg_bytes},
-                "mean_launch_ms": round(mean_launch_ms, 5)}
+                "mean_launch_ms": round(mean_launch_ms, 5), "kernels_per_step": kernels_per_step}
 
     # end to end through the public API with host buffers
     def e2e_line(resident_weights):
@@ -422,7 +427,7 @@ def bench_ours(args):
                            **({"d_offset_bytes": args.d_offset_bytes} if args.d_offset_bytes else {})),
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "e2e_resident_weights": e2e_resident,
-            "gpu_launches": args.steps, "clocks": clk,
+            "gpu_launches": int(round(sum_over_ranks(launches, world, dev))), "clocks": clk,
             "roofline_time_ms": {"tensor_at_peak": tensor_time * 1e3, "hbm_at_peak": hbm_time * 1e3}}
     if rank == 0:
         print(json.dumps(line), flush=True)

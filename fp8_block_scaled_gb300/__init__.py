@@ -50,6 +50,7 @@ from ._binding import (  # noqa: F401
     gemm_grouped_masked_raw,
     gemm_grouped_masked_silu_mul_quant,
     gemm_grouped_masked_silu_mul_quant_raw,
+    kernel_launches,
     lib_path,
     load,
     set_debug_flags,

@@ -34,7 +34,7 @@ EXPORTS = ("gemm_grouped_contiguous", "gemm_grouped_masked", "gemm_grouped_conti
            "gemm_grouped_contiguous_fp32_scales", "gemm_grouped_masked_fp32_scales",
            "gemm_grouped_contiguous_mxfp4", "gemm_grouped_masked_mxfp4",
            "fp8bs_device_error", "fp8bs_status_string", "fp8bs_clear_cache", "fp8bs_abi_version",
-           "fp8bs_set_debug_flags")
+           "fp8bs_set_debug_flags", "fp8bs_kernel_launches")
 
 _lib = None
 _lock = threading.Lock()
@@ -99,6 +99,8 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.fp8bs_set_debug_flags.restype = _I
         lib.fp8bs_abi_version.argtypes = []
         lib.fp8bs_abi_version.restype = _I
+        lib.fp8bs_kernel_launches.argtypes = []
+        lib.fp8bs_kernel_launches.restype = ctypes.c_uint64
         _lib = lib
         return lib
 
@@ -490,3 +492,8 @@ def clear_cache() -> None:
 
 def abi_version() -> int:
     return int(load().fp8bs_abi_version())
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process (a host-side counter)."""
+    return int(load().fp8bs_kernel_launches())

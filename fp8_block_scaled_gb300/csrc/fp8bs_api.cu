@@ -45,6 +45,7 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_launches{0};  // kernels launched (fp8bs_kernel_launches)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 struct MapKey {
@@ -349,6 +350,7 @@ int prepare_scale_images(DeviceState& st, int dev, GemmParams& p, bool masked, c
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     p.sf_a_packed = q.packed_a;
     p.sf_b_packed = q.packed_b;
     p.sf_steps = steps;
@@ -384,6 +386,7 @@ int launch(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUtensor
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return FP8BS_OK;
 }
 
@@ -441,6 +444,7 @@ int launch_pair(DeviceState& st, int attr_slot, const CUtensorMap& ta, const CUt
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return FP8BS_OK;
 }
 
@@ -488,6 +492,7 @@ int launch_promote(DeviceState& st, int attr_slot, const CUtensorMap& ta, const 
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return FP8BS_OK;
 }
 
@@ -633,6 +638,7 @@ int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUte
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return FP8BS_OK;
 }
 
@@ -641,6 +647,8 @@ int launch_pair_noalloc(DeviceState& st, NoAllocDevice& nd, int slot, const CUte
 extern "C" {
 
 int fp8bs_abi_version(void) { return 1; }
+
+uint64_t fp8bs_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int fp8bs_set_debug_flags(uint32_t flags) {
     if (flags & ~(fp8bs::kDebugStallMma | kDebugSingleCta)) return FP8BS_ERR_INVALID_ARG;

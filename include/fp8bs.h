@@ -354,6 +354,15 @@ int fp8bs_set_debug_flags(uint32_t flags);
 /* Library ABI version (1). */
 int fp8bs_abi_version(void);
 
+/* Number of kernels this library has launched in this process, over all
+ * devices and streams: a host-side counter, raised by one for each kernel
+ * launch the CUDA runtime accepted (the scale pre-pass and the GEMM of a call
+ * are two; the counter-clearing cudaMemsetAsync of
+ * gemm_grouped_contiguous_noalloc is not a kernel of the library and does not
+ * count).  A launch captured into a CUDA graph counts once, when captured, not
+ * at each replay.  Never fails. */
+uint64_t fp8bs_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

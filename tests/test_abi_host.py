@@ -100,6 +100,14 @@ def test_contiguous_empty_is_noop(lib):
     assert _contig(m_sum=0, n=100) == INVALID
 
 
+def test_rejected_and_empty_calls_launch_nothing(lib):
+    n0 = fb.kernel_launches()
+    assert _contig(k=100) == INVALID
+    assert _contig(m_sum=0, a=0, d=0) == OK
+    assert _masked(g=0) == INVALID
+    assert fb.kernel_launches() == n0
+
+
 @pytest.mark.parametrize("bad", [
     dict(mm=0), dict(a=0), dict(g=0), dict(g=1025), dict(m_max=-1), dict(n=128 + 64),
     dict(sa_layout=1, ld_sa=63), dict(sa_layout=1, ld_sa=66), dict(out=-1), dict(mm=P + 2),

@@ -306,3 +306,17 @@ def test_named_workload_sampled_rows(gg, name):
         valid, untouched = synth.sample_rows(p, per_group=24, seed=1)
     stats = compare(p, bits, valid, untouched)
     print(name, stats)
+
+
+@pytest.mark.parametrize("sa_layout,kernels", [(SA_MK, 2), (SA_KM, 1)])
+def test_kernels_per_call(gg, sa_layout, kernels):
+    """Row-major activation scales get the scale pre-pass before the GEMM; the
+    transposed layout is read by the GEMM as it is."""
+    p = synth.make_problem("contiguous", 2, 512, 512, [200, 150], sa_layout=sa_layout, seed=58,
+                           device=DEV)
+    run_gpu(p)  # allocates the stream's workspaces
+    n0 = fb.kernel_launches()
+    bits = run_gpu(p)
+    assert fb.kernel_launches() - n0 == kernels
+    valid, untouched = all_rows(p)
+    compare(p, bits, valid, untouched)

@@ -86,7 +86,8 @@ def test_graph_replays_after_the_workspace_grew(gg):
     s = torch.cuda.Stream(priority=-1)  # a stream no earlier call made large workspaces for
     d_small = torch.zeros((small.rows, small.N), dtype=torch.bfloat16, device=DEV)
     d_graph = torch.zeros_like(d_small)
-    d_large = torch.zeros((large.rows, large.N), dtype=torch.bfloat16, device=DEV)
+    d_large = torch.full((large.rows, large.N), SENTINEL, dtype=torch.int16,
+                         device=DEV).view(torch.bfloat16)
     with torch.cuda.stream(s):
         fb.gemm_grouped_contiguous(small.a, small.sa_mk_view(), small.b, small.sb, d_small,
                                    small.grouped_layout)

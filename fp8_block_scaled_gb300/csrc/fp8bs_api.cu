@@ -317,6 +317,7 @@ int prepare_scale_images(DeviceState& st, int dev, GemmParams& p, bool masked, c
     const int64_t tiles = masked ? static_cast<int64_t>(p.num_groups) * p.num_m_tiles : p.num_m_tiles;
     const int64_t a_words = tiles * steps * 128;
     const int64_t b_words = static_cast<int64_t>(p.num_groups) * p.nb_count * steps * 128;
+    if ((a_words + b_words) / 4 >= (int64_t{1} << 31)) return FP8BS_OK;  // 32-bit vector index
     uint32_t* buf = pack_workspace(dev, stream, a_words + b_words);
     if (buf == nullptr) return FP8BS_OK;
     fp8bs::ScalePackParams q{};
@@ -330,13 +331,13 @@ int prepare_scale_images(DeviceState& st, int dev, GemmParams& p, bool masked, c
     q.sa_g_stride = p.sa_g_stride;
     q.sa_kb_stride = p.sa_kb_stride;
     q.sa_row_stride = p.sa_row_stride;
-    q.a_words = a_words;
-    q.b_words = b_words;
+    q.a_vecs = static_cast<uint32_t>(a_words / 4);
+    q.b_vecs = static_cast<uint32_t>(b_words / 4);
     q.kb_count = p.kb_count;
     q.steps = steps;
     q.tiles_per_group = p.num_m_tiles;
     q.masked = masked ? 1 : 0;
-    const int64_t blocks = (a_words + b_words + 255) / 256;
+    const int64_t blocks = ((a_words + b_words) / 4 + 255) / 256;
     const int64_t max_blocks = static_cast<int64_t>(st.sms) * 8;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];

@@ -34,84 +34,94 @@ struct ScalePackParams {
     const float* sa;
     const float* sb;
     const int32_t* row_info;   // contiguous: grouped_layout [rows]; masked: masked_m [G]
-    uint32_t* packed_a;
-    uint32_t* packed_b;
+    uint32_t* packed_a;        // 16-byte aligned
+    uint32_t* packed_b;        // 16-byte aligned
     uint32_t* err;
     int64_t rows;              // contiguous: m_sum; masked: m_max
     int64_t sa_g_stride, sa_kb_stride, sa_row_stride;
-    int64_t a_words;           // tiles * steps * 128
-    int64_t b_words;           // G * N/128 * steps * 128
+    uint32_t a_vecs;           // 16-byte vectors of packed A: tiles * steps * 32
+    uint32_t b_vecs;           // 16-byte vectors of packed B: G * N/128 * steps * 32
     int kb_count, steps, tiles_per_group, masked;
 };
 
-__device__ __forceinline__ uint32_t ue8m0_code(uint32_t fbits) { return (fbits >> 23) & 0xFFu; }
+// the UE8M0 codes of K blocks 2 ks and 2 ks + 1 as one image word: bytes c0, c1, c0, c1
+__device__ __forceinline__ uint32_t image_word(uint32_t f0, uint32_t f1) {
+    return (((f0 >> 23) & 0xFFu) | (((f1 >> 23) & 0xFFu) << 8)) * 0x00010001u;
+}
 
+// A warp writes one 512-byte image at a time, lane l one 16-byte vector of it: four
+// words of a (tile, step) image, rows l, 32 + l, 64 + l and 96 + l of the tile
+// (words 4 l .. 4 l + 3), or four copies of a weight-scale word.  Consecutive images
+// go to consecutive blocks, so that the activation images (gathers of scattered
+// rows, the costly part) are spread over every block and SM rather than left to
+// the first few.
 __global__ void __launch_bounds__(256) scale_pack_kernel(const ScalePackParams p) {
     // the scales may be written by the grid this launch follows, and the workspace
     // may still be read by it (programmatic dependent launch)
     grid_dependency_wait();
     grid_launch_dependents();
-    const int64_t total = p.a_words + p.b_words;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const uint32_t images = (p.a_vecs + p.b_vecs) >> 5;
+    const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+    const uint32_t steps = static_cast<uint32_t>(p.steps);
+    const uint32_t lane = threadIdx.x & 31u;
     bool bad = false;
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < total;
-         w += stride) {
-        if (w < p.a_words) {
-            const int64_t tk = w >> 7;              // (tile, step)
-            const int pos = static_cast<int>(w & 127);
-            const int64_t t = tk / p.steps;
-            const int ks = static_cast<int>(tk - t * p.steps);
-            const int r = (pos & 3) * 32 + (pos >> 2);
-            int64_t m, sa_goff = 0;
-            int g = 0;
+    for (uint32_t img = (threadIdx.x >> 5) * gridDim.x + blockIdx.x; img < images; img += warps) {
+        const uint32_t v = img * 32u + lane;
+        if (v < p.a_vecs) {
+            const uint32_t tk = v >> 5;                    // (tile, step)
+            const uint32_t t = tk / steps;
+            const int ks = static_cast<int>(tk - t * steps);
+            const int l = static_cast<int>(v & 31u);
+            int64_t m0, sa_goff = 0;
+            int mm = 0, tg = 0;
             if (p.masked) {
-                g = static_cast<int>(t / p.tiles_per_group);
-                m = (t - static_cast<int64_t>(g) * p.tiles_per_group) * kBM + r;
+                const uint32_t g = t / static_cast<uint32_t>(p.tiles_per_group);
+                m0 = static_cast<int64_t>(t - g * p.tiles_per_group) * kBM;
+                mm = __ldg(p.row_info + g);
+                mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
+                // no unit reads a tile past masked_m[g] (the second tile of a pair
+                // whose first one holds rows is read, by its idle half): not written
+                if (!(m0 < mm || (m0 >= kBM && m0 - kBM < mm))) continue;
                 sa_goff = static_cast<int64_t>(g) * p.sa_g_stride;
             } else {
-                m = t * kBM + r;
+                m0 = static_cast<int64_t>(t) * kBM;
+                tg = __ldg(p.row_info + m0);               // the tile's group
             }
-            // images of masked tiles that no unit reads (past masked_m[g]) are not
-            // written
-            bool used, stored = false;
-            if (p.masked) {
-                int mm = __ldg(p.row_info + g);
-                mm = mm < 0 ? 0 : (mm > p.rows ? static_cast<int>(p.rows) : mm);
-                const int64_t tile_m0 = (t - static_cast<int64_t>(g) * p.tiles_per_group) * kBM;
-                used = tile_m0 < mm || (tile_m0 >= kBM && tile_m0 - kBM < mm);  // or a pair's idle half
-                stored = m < mm;
-            } else {
-                const int tg = __ldg(p.row_info + t * kBM);
-                used = true;  // the idle half of an odd pair reads the tile after it
-                stored = m < p.rows && tg >= 0 && __ldg(p.row_info + m) == tg;
-            }
-            if (!used) continue;
-            uint32_t code[2];
+            uint32_t f[4][2];
+            bool stored[4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int kb = 2 * ks + j;
-                uint32_t v = 0;
-                if (m < p.rows && kb < p.kb_count) {
-                    v = __float_as_uint(
-                        __ldg(p.sa + sa_goff + kb * p.sa_kb_stride + m * p.sa_row_stride));
-                    bad |= stored && !ue8m0_scale_ok(v);
+            for (int q = 0; q < 4; ++q) {
+                const int64_t m = m0 + q * 32 + l;
+                const bool in = m < p.rows;
+                stored[q] = p.masked ? m < mm : in && tg >= 0 && __ldg(p.row_info + m) == tg;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int kb = 2 * ks + j;
+                    f[q][j] = in && kb < p.kb_count
+                                  ? __float_as_uint(__ldg(p.sa + sa_goff + kb * p.sa_kb_stride +
+                                                          m * p.sa_row_stride))
+                                  : 0u;
                 }
-                code[j] = ue8m0_code(v);
             }
-            p.packed_a[w] = code[0] | (code[1] << 8) | (code[0] << 16) | (code[1] << 24);
-        } else {
-            const int64_t wb = w - p.a_words;
-            const int64_t ck = wb >> 7;             // (g * N/128 + nb, step)
-            const int64_t c = ck / p.steps;
-            const int ks = static_cast<int>(ck - c * p.steps);
-            uint32_t code[2];
+            uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int kb = 2 * ks + j;
-                code[j] = kb < p.kb_count ? ue8m0_code(__float_as_uint(__ldg(p.sb + c * p.kb_count + kb)))
-                                          : 0u;
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    bad |= stored[q] && 2 * ks + j < p.kb_count && !ue8m0_scale_ok(f[q][j]);
+                w[q] = image_word(f[q][0], f[q][1]);
             }
-            p.packed_b[wb] = code[0] | (code[1] << 8) | (code[0] << 16) | (code[1] << 24);
+            st_global_v4(p.packed_a + static_cast<int64_t>(v) * 4, w[0], w[1], w[2], w[3]);
+        } else {
+            const uint32_t vb = v - p.a_vecs;
+            const uint32_t ck = vb >> 5;                   // (g * N/128 + nb, step)
+            const uint32_t c = ck / steps;
+            const int ks = static_cast<int>(ck - c * steps);
+            const float* src = p.sb + static_cast<int64_t>(c) * p.kb_count + 2 * ks;
+            const uint32_t f0 = __float_as_uint(__ldg(src));
+            const uint32_t f1 = 2 * ks + 1 < p.kb_count ? __float_as_uint(__ldg(src + 1)) : 0u;
+            const uint32_t w = image_word(f0, f1);
+            st_global_v4(p.packed_b + static_cast<int64_t>(vb) * 4, w, w, w, w);
         }
     }
     if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) raise_error(p.err, kErrBadScale);

@@ -105,7 +105,9 @@ SkWorkspace* sk_workspace(int dev, cudaStream_t stream, int slots) {
 
 // Buffers of the per-stream workspaces below that a larger call replaced.  They are
 // kept, not freed, until the process exits: a CUDA graph captured while one of them
-// was current still points at it.  Growth at least doubles a workspace, so the kept
+// was current still points at it.  A workspace is allocated at twice the size its
+// call needs and grows to at least twice its size, so calls of varying sizes (the
+// row count of a MoE layer changes with every batch) seldom allocate, and the kept
 // buffers add up to less than the current one.
 std::vector<void*> g_retired;
 
@@ -135,7 +137,7 @@ bool pair_list_workspace(int dev, cudaStream_t stream, int ctas, int64_t m_tiles
             cudaGetLastError();
             return false;
         }
-        const int64_t size = it == g_list.end() ? ints : std::max(ints, 2 * it->second.ints);
+        const int64_t size = std::max(2 * ints, it == g_list.end() ? 0 : 2 * it->second.ints);
         ListWorkspace w;
         if (cudaMalloc(&w.buf, sizeof(int) * size) != cudaSuccess) {
             cudaGetLastError();
@@ -177,7 +179,7 @@ uint32_t* pack_workspace(int dev, cudaStream_t stream, int64_t words) {
         cudaGetLastError();
         return nullptr;
     }
-    const int64_t size = it == g_pack.end() ? words : std::max(words, 2 * it->second.words);
+    const int64_t size = std::max(2 * words, it == g_pack.end() ? 0 : 2 * it->second.words);
     PackWorkspace w;
     if (cudaMalloc(&w.buf, sizeof(uint32_t) * size) != cudaSuccess) {
         cudaGetLastError();

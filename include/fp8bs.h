@@ -63,9 +63,10 @@
  *    third per-stream workspace of (128-row tiles + num_groups * n/128) *
  *    ceil(k/256) * 512 bytes, allocated the same way.  When it cannot be had
  *    the GEMM converts the fp32 scales itself (same results).
- *  - A per-stream workspace that a larger call outgrows is replaced by one at
- *    least twice its size; the old buffer is kept, not freed, until exit, so a
- *    CUDA graph captured while it was current stays valid.  A graph keeps
+ *  - A per-stream workspace is allocated at twice the size its call needs; a
+ *    larger call that outgrows it replaces it by one at least twice its size,
+ *    and the old buffer is kept, not freed, until exit, so a CUDA graph
+ *    captured while it was current stays valid.  A graph keeps
  *    using the workspaces of the stream it was captured on: do not replay it
  *    on another stream while calls run on that one.
  *  - Kernels: gemm_grouped_contiguous and gemm_grouped_masked run a CTA-pair

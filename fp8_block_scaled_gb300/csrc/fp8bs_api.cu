@@ -67,6 +67,26 @@ struct SkWorkspace {
     uint32_t* flags = nullptr;
     int slots = 0;
 };
+// Buffers of the per-stream workspaces below that a larger call replaced.  They are
+// kept, not freed, until the process exits: a CUDA graph captured while one of them
+// was current still points at it.  The pair list and the scale images are allocated
+// at twice the size their call needs and grow to at least twice their size, so calls
+// of varying sizes (the row count of a MoE layer changes with every batch) seldom
+// allocate, and the kept buffers add up to less than the current ones.
+std::vector<void*> g_retired;
+
+// cudaMalloc with this thread's stream-capture mode relaxed for the call.  Callers
+// never allocate while the call's own stream is capturing; a capture in global mode
+// on another stream (torch's default) would otherwise make the allocation fail and
+// invalidate that capture.
+cudaError_t malloc_outside_capture(void** ptr, size_t bytes) {
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    const cudaError_t e = cudaMalloc(ptr, bytes);
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    return e;
+}
+
 std::map<std::pair<int, void*>, SkWorkspace> g_sk;
 constexpr size_t kSkSlotBytes = 128 * 256 * sizeof(float);
 
@@ -82,34 +102,27 @@ SkWorkspace* sk_workspace(int dev, cudaStream_t stream, int slots) {
         cudaGetLastError();
         return nullptr;
     }
-    if (it != g_sk.end()) {
-        cudaStreamSynchronize(stream);
-        cudaFree(it->second.partial);
-        cudaFree(it->second.flags);
-        g_sk.erase(it);
-    }
     SkWorkspace w;
-    if (cudaMalloc(&w.partial, kSkSlotBytes * slots) != cudaSuccess) {
+    if (malloc_outside_capture(reinterpret_cast<void**>(&w.partial), kSkSlotBytes * slots) !=
+        cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }
-    if (cudaMalloc(&w.flags, 2 * sizeof(uint32_t) * slots) != cudaSuccess ||
+    if (malloc_outside_capture(reinterpret_cast<void**>(&w.flags), 2 * sizeof(uint32_t) * slots) !=
+            cudaSuccess ||
         cudaMemsetAsync(w.flags, 0, 2 * sizeof(uint32_t) * slots, stream) != cudaSuccess) {
         cudaGetLastError();
-        cudaFree(w.partial);
+        g_retired.push_back(w.partial);  // not freed: cudaFree is as unsafe during a capture
+        if (w.flags != nullptr) g_retired.push_back(w.flags);
         return nullptr;
     }
     w.slots = slots;
+    if (it != g_sk.end()) {  // a grid with more pairs than the stream's earlier launches
+        g_retired.push_back(it->second.partial);
+        g_retired.push_back(it->second.flags);
+    }
     return &(g_sk[key] = w);
 }
-
-// Buffers of the per-stream workspaces below that a larger call replaced.  They are
-// kept, not freed, until the process exits: a CUDA graph captured while one of them
-// was current still points at it.  A workspace is allocated at twice the size its
-// call needs and grows to at least twice its size, so calls of varying sizes (the
-// row count of a MoE layer changes with every batch) seldom allocate, and the kept
-// buffers add up to less than the current one.
-std::vector<void*> g_retired;
 
 // Device pair list of a contiguous problem whose row tiles outnumber the kernel's
 // shared-memory list: one region of `stride` ints per CTA of a grid of at most `ctas`
@@ -139,7 +152,7 @@ bool pair_list_workspace(int dev, cudaStream_t stream, int ctas, int64_t m_tiles
         }
         const int64_t size = std::max(2 * ints, it == g_list.end() ? 0 : 2 * it->second.ints);
         ListWorkspace w;
-        if (cudaMalloc(&w.buf, sizeof(int) * size) != cudaSuccess) {
+        if (malloc_outside_capture(reinterpret_cast<void**>(&w.buf), sizeof(int) * size) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
@@ -181,7 +194,7 @@ uint32_t* pack_workspace(int dev, cudaStream_t stream, int64_t words) {
     }
     const int64_t size = std::max(2 * words, it == g_pack.end() ? 0 : 2 * it->second.words);
     PackWorkspace w;
-    if (cudaMalloc(&w.buf, sizeof(uint32_t) * size) != cudaSuccess) {
+    if (malloc_outside_capture(reinterpret_cast<void**>(&w.buf), sizeof(uint32_t) * size) != cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }

@@ -3,7 +3,9 @@ has already run the op (so its stream-K workspace exists) replays to the same
 bits as the eager launch, and the masked variant replays correctly too.  The
 per-stream workspaces (stream-K scratch, scale images of row-major activation
 scales) are not allocated during a capture, and one that a later, larger call
-on the stream grows keeps the buffer an earlier capture points at."""
+on the stream grows keeps the buffer an earlier capture points at.  A call on
+another stream may allocate its workspaces while a graph is being captured in
+torch's default (global) capture mode without breaking that capture."""
 import numpy as np
 import pytest
 import torch
@@ -108,3 +110,33 @@ def test_graph_replays_after_the_workspace_grew(gg):
     assert fb.device_error() == 0
     valid, untouched = all_rows(large)
     compare(large, _bits(d_large), valid, untouched)
+
+
+def test_first_call_on_a_stream_while_another_stream_captures(gg):
+    p = synth.make_problem("contiguous", 2, 512, 512, [200, 150], seed=706, device=DEV)
+
+    def sentinel():
+        return torch.full((p.rows, p.N), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+
+    def call(d, stream=None):
+        fb.gemm_grouped_contiguous(p.a, p.sa_mk_view(), p.b, p.sb, d, p.grouped_layout, stream=stream)
+
+    d_ref, d_graph, d_other = sentinel(), sentinel(), sentinel()
+    call(d_ref)  # 4 units: no stream-K split, so every stream gives the same bits
+    torch.cuda.synchronize()
+    s_cap = torch.cuda.Stream(priority=-1)
+    s_new = torch.cuda.Stream(priority=-1)  # no call has run on it yet
+    with torch.cuda.stream(s_cap):
+        call(d_graph)  # the capturing stream's workspaces exist before the capture
+    s_cap.synchronize()
+    d_graph.view(torch.int16).fill_(SENTINEL)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s_cap):  # capture_error_mode="global"
+        call(d_graph)
+        call(d_other, stream=s_new)  # eager, allocates s_new's workspaces
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fb.device_error() == 0
+    assert np.array_equal(_bits(d_graph), _bits(d_ref))
+    assert np.array_equal(_bits(d_other), _bits(d_ref))

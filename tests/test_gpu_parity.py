@@ -184,20 +184,23 @@ def test_device_flags_mixed_and_bad_groups(gg, d_offset, single):
     assert fb.device_error() == 0  # cleared by the read
 
 
+@pytest.mark.parametrize("sa_layout", [SA_MK, SA_KM])
 @pytest.mark.parametrize("n", [512, 384])
 @pytest.mark.parametrize("variant", ["contiguous", "masked"])
-def test_single_cta_and_pair_kernels_agree(gg, variant, n):
-    """The same N%256==0 problem through the CTA-pair kernel with a 32-byte and a
-    16-byte aligned D (one 32-byte store or two 16-byte stores per 16 columns) and
-    through the single-CTA kernel, each against the oracle; the two pair runs are
-    bit-identical and the words around D are never written."""
+def test_single_cta_and_pair_kernels_agree(gg, variant, n, sa_layout):
+    """The same problem through the CTA-pair kernel with a 32-byte and a 16-byte
+    aligned D (one 32-byte store or two 16-byte stores per 16 columns) and through
+    the single-CTA kernel, each against the oracle; the two pair runs are
+    bit-identical and the words around D are never written.  With row-major
+    activation scales the pair kernel reads the scale pre-pass's images, the
+    single-CTA kernel converts the scales itself."""
     if variant == "contiguous":
-        p = synth.make_problem("contiguous", 3, n, 768, [100, 300, 257], sa_layout=SA_KM,
+        p = synth.make_problem("contiguous", 3, n, 768, [100, 300, 257], sa_layout=sa_layout,
                                seed=93, device=DEV)
         shape = (p.rows, p.N)
     else:
-        p = synth.make_problem("masked", 3, n, 768, [100, 300, 257], M_max=320, sa_layout=SA_KM,
-                               seed=94, device=DEV)
+        p = synth.make_problem("masked", 3, n, 768, [100, 300, 257], M_max=320,
+                               sa_layout=sa_layout, seed=94, device=DEV)
         shape = (p.G, p.M_max, p.N)
     numel = p.rows * p.N
     outs = []
@@ -320,3 +323,22 @@ def test_kernels_per_call(gg, sa_layout, kernels):
     assert fb.kernel_launches() - n0 == kernels
     valid, untouched = all_rows(p)
     compare(p, bits, valid, untouched)
+
+
+def test_varying_sizes_on_one_stream(gg):
+    """Calls of growing and shrinking sizes on one stream, as a MoE layer sees them
+    batch after batch: the stream's workspaces (stream-K scratch, scale images)
+    grow and are reused, and every call meets the tolerances on every row."""
+    rng = np.random.default_rng(59)
+    s = torch.cuda.Stream(priority=-1)
+    for i, rows in enumerate([64, 900, 200, 2500, 40, 1300]):
+        G = 4
+        sizes = [int(v) for v in rng.multinomial(rows, [0.4, 0.3, 0.2, 0.1])]
+        K = [512, 1024, 768][i % 3]
+        sa_layout = SA_MK if i % 2 == 0 else SA_KM
+        p = synth.make_problem("contiguous", G, 512, K, sizes, sa_layout=sa_layout, seed=600 + i,
+                               device=DEV)
+        with torch.cuda.stream(s):
+            bits = run_gpu(p, stream=s)
+        valid, untouched = all_rows(p)
+        compare(p, bits, valid, untouched, check_fp32=False)

@@ -304,8 +304,7 @@ int gemm_grouped_masked_mxfp4(const void* a, const uint8_t* scale_a, const void*
  *    holds it until the process exits.  A device that fits more than 80 CTA
  *    pairs runs this entry point on 80 of them (same results);
  *  - the first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before capturing the stream into a CUDA graph;
+ *    (cudaGetSymbolAddress) with that device current;
  *  - every call clears the slot counters (cudaMemsetAsync on `stream`) and
  *    then launches, so unlike the other entry points its kernel does not
  *    start early on SMs freed by the preceding kernel on the stream; calls

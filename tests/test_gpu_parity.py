@@ -342,3 +342,22 @@ def test_varying_sizes_on_one_stream(gg):
             bits = run_gpu(p, stream=s)
         valid, untouched = all_rows(p)
         compare(p, bits, valid, untouched, check_fp32=False)
+
+
+@pytest.mark.parametrize("sa_layout", [SA_MK, SA_KM], ids=["sa_mk", "sa_km"])
+@pytest.mark.parametrize("n", [128, 384])
+@pytest.mark.parametrize("k", [128, 256, 384])
+@pytest.mark.parametrize("variant", ["contiguous", "masked"])
+def test_smallest_shapes(gg, variant, k, n, sa_layout):
+    """The fewest K blocks (one: a pipeline step with an empty second slot; two: one
+    step; three: a step and a half) and the narrowest column tiles (N = 128: one
+    128-column tile; N = 384: a full tile and a 128-column one), ragged rows."""
+    if variant == "contiguous":
+        p = synth.make_problem("contiguous", 3, n, k, [1, 130, 77], sa_layout=sa_layout,
+                               seed=70 + k // 128 + n, device=DEV, tail_rows=9)
+    else:
+        p = synth.make_problem("masked", 3, n, k, [1, 130, 0], M_max=140, sa_layout=sa_layout,
+                               seed=80 + k // 128 + n, device=DEV)
+    bits = run_gpu(p)
+    valid, untouched = all_rows(p)
+    compare(p, bits, valid, untouched)

@@ -153,6 +153,9 @@ int gemm_grouped_contiguous(const void* a, const float* scale_a, int sa_layout, 
  *              (values outside are clamped and flagged FP8BS_DEVERR_MASKED_M)
  *   expected_m a hint of the typical masked_m; it never changes results (may be 0)
  *   d          out_dtype [num_groups, m_max, n]
+ *   1 <= num_groups <= 1024 (the kernels keep a prefix over the groups in shared
+ *   memory; FP8BS_ERR_INVALID_ARG above), m_max >= 0, n and k as for the
+ *   contiguous variant.
  */
 int gemm_grouped_masked(const void* a, const float* scale_a, int sa_layout, int64_t ld_sa,
                         const void* b, const float* scale_b, const int32_t* masked_m,
@@ -273,7 +276,8 @@ int gemm_grouped_masked_fp32_scales(const void* a, const float* scale_a, int sa_
  *   d        out_dtype [m_sum, n] or [num_groups, m_max, n], 32-byte aligned
  *   n % 256 == 0, k % 256 == 0; contiguous: m_sum <= 4194304 rows, num_groups
  *   < 2^15 (above 507904 rows the pair list lives in the per-stream device
- *   workspace, FP8BS_ERR_CUDA if it would have to grow during stream capture).
+ *   workspace, FP8BS_ERR_CUDA if it would have to grow during stream capture);
+ *   masked: num_groups <= 1024.
  *   grouped_layout / masked_m / expected_m as for the E4M3 variants.
  * Runs on the CTA-pair kernel (with the stream-K tail for the contiguous
  * variant).

@@ -259,7 +259,7 @@ def test_fp32_scales_masked_rejects_and_empty(lib):
             args["a"], args["sa"], args["sa_layout"], args["ld_sa"], args["b"], args["sb"],
             args["mm"], 0, args["d"], args["out"], args["g"], args["m_max"], args["n"],
             args["k"], 0)
-    for bad in (dict(n=384), dict(d=P + 16), dict(mm=0), dict(g=0), dict(m_max=-1)):
+    for bad in (dict(n=384), dict(d=P + 16), dict(mm=0), dict(g=0), dict(g=1025), dict(m_max=-1)):
         assert call(**bad) == INVALID, bad
     assert call(m_max=0, a=0) == OK
     assert _fp32s(m_sum=0, a=0, d=0) == OK

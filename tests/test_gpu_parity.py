@@ -55,11 +55,12 @@ def test_contiguous_wide_n_tiles(gg, sa_layout):
     compare(p, bits, valid, untouched)
 
 
+@pytest.mark.parametrize("out", [OUT_BF16, OUT_F16])
 @pytest.mark.parametrize("sa_layout", [SA_MK, SA_KM])
 @pytest.mark.parametrize("n", [256, 384])
-def test_masked_ragged(gg, sa_layout, n):
+def test_masked_ragged(gg, sa_layout, n, out):
     """M_max=200 (not a multiple of 128); masked_m = 0, 1, 200 (full) and 129."""
-    p = synth.make_problem("masked", 4, n, 384, [0, 1, 200, 129], M_max=200,
+    p = synth.make_problem("masked", 4, n, 384, [0, 1, 200, 129], M_max=200, out_dtype=out,
                            sa_layout=sa_layout, seed=51, device=DEV)
     bits = run_gpu(p)
     valid, untouched = all_rows(p)
@@ -361,3 +362,20 @@ def test_smallest_shapes(gg, variant, k, n, sa_layout):
     bits = run_gpu(p)
     valid, untouched = all_rows(p)
     compare(p, bits, valid, untouched)
+
+
+def test_expected_m_never_changes_results(gg):
+    """expected_m is a hint of the typical masked_m (DeepGEMM's masked contract, as
+    "Adds Grouped and Batched GEMM kernels with blockscaling matching DeepGEMM API",
+    Summary, adopts it): any value gives the same bits."""
+    p = synth.make_problem("masked", 3, 256, 256, [10, 200, 0], M_max=256, seed=59, device=DEV)
+    outs = []
+    for em in (0, 1, 128, 1 << 20):
+        d = torch.full((p.G, p.M_max, p.N), SENTINEL, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        fb.gemm_grouped_masked(p.a, p.sa_mk_view(), p.b, p.sb, d, p.masked_m, em)
+        torch.cuda.synchronize()
+        assert fb.device_error() == 0
+        outs.append(d.view(torch.int16).cpu().numpy())
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    valid, untouched = all_rows(p)
+    compare(p, outs[0].view(np.uint16).reshape(-1, p.N), valid, untouched)
